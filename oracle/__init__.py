@@ -245,3 +245,76 @@ def e4m3_output_ref(y_ref, out_scale) -> np.ndarray:
     quotient kept in float64 (no intermediate float32 rounding)."""
     y = np.asarray(y_ref, dtype=np.float64)
     return e4m3_encode(y / np.float64(np.float32(out_scale)))
+
+
+# --------------------------------------------------------------------------
+# parity criteria (used by the tests, the smoke check and the benchmark)
+
+GEMM_ELEMENT_TOL = 1e-2   # |y - y_ref| <= 1e-2 (|y_ref| + rms(y_ref)) per element
+GEMM_FRO_TOL = 5e-3       # ||y - y_ref||_F <= 5e-3 ||y_ref||_F
+E4M3_FRO_TOL = 2.0 ** -4  # E4M3 output: half the relative code spacing
+E4M3_MIDPOINT_WINDOW = 1e-3
+
+
+def gemm_close(y, y_ref) -> dict:
+    """Tolerance of a 16-bit GEMM output against the float64 reference of
+    the same FP8 operands: elementwise ``|y - y_ref| <= 1e-2 (|y_ref| +
+    rms(y_ref))`` and relative Frobenius error ``<= 5e-3``."""
+    y = np.asarray(y, dtype=np.float64)
+    y_ref = np.asarray(y_ref, dtype=np.float64)
+    assert y.shape == y_ref.shape
+    if y.size == 0:
+        return {"ok": True, "max_ratio": 0.0, "rel_fro": 0.0}
+    rms = float(np.sqrt(np.mean(y_ref ** 2)))
+    err = np.abs(y - y_ref)
+    bound = GEMM_ELEMENT_TOL * (np.abs(y_ref) + rms)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(bound > 0, err / bound, np.where(err > 0, np.inf, 0.0))
+    max_ratio = float(np.max(ratio))
+    nref = float(np.linalg.norm(y_ref))
+    rel_fro = float(np.linalg.norm(y - y_ref) / nref) if nref > 0 else float(np.linalg.norm(y))
+    ok = bool(np.all(np.isfinite(y))) and max_ratio <= 1.0 and rel_fro <= GEMM_FRO_TOL
+    return {"ok": ok, "max_ratio": max_ratio, "rel_fro": rel_fro}
+
+
+def _signed_ordinal(codes):
+    c = np.asarray(codes, dtype=np.int64)
+    mag = c & 0x7F
+    return np.where(c & 0x80, -mag, mag)
+
+
+def _nearest_midpoint_distance(t):
+    pos = decode_table()[:127]
+    mids = (pos[:-1] + pos[1:]) / 2
+    a = np.minimum(np.abs(t), 448.0)
+    i = np.clip(np.searchsorted(mids, a), 1, len(mids) - 1)
+    return np.minimum(np.abs(a - mids[i - 1]), np.abs(a - mids[i]))
+
+
+def e4m3_output_close(codes, y_ref, out_scale) -> dict:
+    """Tolerance of an E4M3 GEMM output (codes) against y_ref.
+
+    Reading (the stated GEMM tolerance is finer than E4M3 can resolve):
+    c_ref = E4M3(y_ref / out_scale) in float64; every code is within one
+    step of c_ref on the signed code ordinal (0x00 and 0x80 equal);
+    codes equal c_ref wherever t = y_ref / out_scale lies farther than
+    1e-3 (|t| + rms(t)) from a rounding midpoint; and
+    ||dec(code) - clip(t)||_F <= 2^-4 ||clip(t)||_F with clip to +-448
+    (the saturated reference)."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    y_ref = np.asarray(y_ref, dtype=np.float64)
+    os_ = np.float64(np.float32(out_scale))
+    t = y_ref / os_
+    c_ref = e4m3_encode(t)
+    step = np.abs(_signed_ordinal(codes) - _signed_ordinal(c_ref))
+    rms = float(np.sqrt(np.mean(t ** 2))) if t.size else 0.0
+    far = _nearest_midpoint_distance(t) > E4M3_MIDPOINT_WINDOW * (np.abs(t) + rms)
+    exact_bad = int(np.count_nonzero(far & (_signed_ordinal(codes) != _signed_ordinal(c_ref))))
+    tc = np.clip(t, -448.0, 448.0)
+    dec = decode_table()[codes]
+    nref = float(np.linalg.norm(tc))
+    rel_fro = float(np.linalg.norm(dec - tc) / nref) if nref > 0 else float(np.linalg.norm(dec))
+    max_step = int(step.max()) if step.size else 0
+    ok = max_step <= 1 and exact_bad == 0 and rel_fro <= E4M3_FRO_TOL and not np.any(np.isnan(dec))
+    return {"ok": ok, "max_step": max_step, "exact_mismatch": exact_bad, "rel_fro": rel_fro,
+            "differing": int(np.count_nonzero(step))}

@@ -52,6 +52,20 @@ void fp8o_e4m3_decode_table(double out[256])
         out[c] = fp8o_e4m3_decode(c);
 }
 
+/* The same 256 values, computed once by fp8o_e4m3_decode and kept for the
+ * loops below (a cache, not a second definition). */
+static double g_value[256];
+static int g_value_ready = 0;
+
+static const double *value_table(void)
+{
+    if (!g_value_ready) {
+        fp8o_e4m3_decode_table(g_value);
+        g_value_ready = 1;
+    }
+    return g_value;
+}
+
 /* Saturating round-to-nearest-even encode of a real value.
  *
  * The 127 non-negative finite codes 0x00..0x7E have strictly increasing
@@ -64,6 +78,7 @@ void fp8o_e4m3_decode_table(double out[256])
  * is outside the layer's contract).                                        */
 unsigned fp8o_e4m3_encode(double v)
 {
+    const double *val = value_table();
     unsigned sign, lo, hi;
     double a, mid;
     if (v != v)
@@ -77,12 +92,12 @@ unsigned fp8o_e4m3_encode(double v)
     hi = 0x7Eu;
     while (hi - lo > 1u) {
         unsigned m = (lo + hi) / 2u;
-        if (fp8o_e4m3_decode(m) <= a)
+        if (val[m] <= a)
             lo = m;
         else
             hi = m;
     }
-    mid = 0.5 * (fp8o_e4m3_decode(lo) + fp8o_e4m3_decode(hi));
+    mid = 0.5 * (val[lo] + val[hi]);
     if (a < mid)
         return sign | lo;
     if (a > mid)
@@ -162,12 +177,12 @@ void fp8o_scaled_mm_f64(const uint8_t *qa, const uint8_t *qw,
                         float sa, const float *sw, int per_channel,
                         double *y)
 {
+    const double *val = value_table();
     for (int64_t m = 0; m < M; ++m) {
         for (int64_t n = 0; n < N; ++n) {
             double acc = 0.0;
             for (int64_t k = 0; k < K; ++k)
-                acc += fp8o_e4m3_decode(qa[m * K + k]) *
-                       fp8o_e4m3_decode(qw[n * K + k]);
+                acc += val[qa[m * K + k]] * val[qw[n * K + k]];
             double wscale = per_channel ? (double)sw[n] : (double)sw[0];
             y[m * N + n] = ((double)sa * wscale) * acc;
         }
@@ -181,11 +196,12 @@ void fp8o_scaled_mm_f64(const uint8_t *qa, const uint8_t *qw,
 void fp8o_w8a16_mm_f64(const float *x, const uint8_t *qw, const float *sw,
                        int64_t M, int64_t N, int64_t K, double *y)
 {
+    const double *val = value_table();
     for (int64_t m = 0; m < M; ++m) {
         for (int64_t n = 0; n < N; ++n) {
             double acc = 0.0;
             for (int64_t k = 0; k < K; ++k)
-                acc += (double)x[m * K + k] * fp8o_e4m3_decode(qw[n * K + k]);
+                acc += (double)x[m * K + k] * val[qw[n * K + k]];
             y[m * N + n] = (double)sw[n] * acc;
         }
     }
