@@ -1,0 +1,17 @@
+"""FP8 E4M3 quantized linear layer for NVIDIA GB300 (sm_103a).
+
+A C-ABI library (``libfp8linear.so``, declared in ``include/fp8linear.h``)
+with hand-written CUDA kernels, and a thin ctypes binding whose functions
+carry the C entry points' names:
+
+  fp8_quant_per_tensor  dynamic or static per-tensor quantization to E4M3
+  fp8_quant_per_row     per-output-channel weight quantization (setup)
+  fp8_scaled_mm         W8A8 scaled product (tcgen05 GEMM; M <= 16 streams W)
+  fp8_w8a16_mm          weight-only fp16/bf16 x E4M3 product
+
+The library is loaded on first use; nothing here computes on the CPU.
+"""
+from ._binding import (  # noqa: F401
+    BF16, E4M3, F16, F32, Fp8LinearError, LIB_PATH, fp8_quant_per_row,
+    fp8_quant_per_tensor, fp8_scaled_mm, fp8_w8a16_mm, fp8l_read_status,
+    fp8l_workspace_bytes, load, strerror, workspace)

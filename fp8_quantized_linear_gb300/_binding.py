@@ -1,0 +1,206 @@
+"""ctypes binding of libfp8linear.so: argument marshalling only.
+
+Every function has the name of the C entry point it calls.  Tensors are torch
+CUDA tensors (torch supplies device memory and the current stream); E4M3
+tensors are uint8 code tensors (a torch.float8_e4m3fn tensor is accepted and
+viewed as uint8).  Every step of the computation runs in the library's CUDA
+kernels; there is no CPU or PyTorch fallback, and a missing library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfp8linear.so")
+
+F16, BF16, E4M3, F32 = 0, 1, 2, 3
+OK, EINVAL, ESHAPE, EALIGN, ECUDA, ETIMEOUT, EUNSUPPORTED = range(7)
+
+_DTYPE_CODE = {torch.float16: F16, torch.bfloat16: BF16, torch.float32: F32,
+               torch.uint8: E4M3, torch.float8_e4m3fn: E4M3}
+_CODE_DTYPE = {F16: torch.float16, BF16: torch.bfloat16, E4M3: torch.uint8}
+
+_lock = threading.Lock()
+_lib = None
+_workspaces = {}
+
+
+class Fp8LinearError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {strerror(status)} (status {status})")
+
+
+def load():
+    """The loaded library (ctypes.CDLL); raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; "
+                f"g.build()\"` (nvcc, sm_103a)")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        lib.fp8l_workspace_bytes.restype = ctypes.c_size_t
+        lib.fp8l_workspace_bytes.argtypes = []
+        lib.fp8l_abi_version.restype = I
+        lib.fp8l_strerror.restype = ctypes.c_char_p
+        lib.fp8l_strerror.argtypes = [I]
+        lib.fp8l_read_status.restype = I
+        lib.fp8l_read_status.argtypes = [P, P]
+        lib.fp8_quant_per_tensor.restype = I
+        lib.fp8_quant_per_tensor.argtypes = [P, I, I64, I64, P, P, I, P, P]
+        lib.fp8_quant_per_row.restype = I
+        lib.fp8_quant_per_row.argtypes = [P, I, I64, I64, P, P, P]
+        lib.fp8_scaled_mm.restype = I
+        lib.fp8_scaled_mm.argtypes = [P, P, I64, I64, I64, P, P, I, P, P, I, P, P]
+        lib.fp8_w8a16_mm.restype = I
+        lib.fp8_w8a16_mm.argtypes = [P, I, P, P, I64, I64, I64, P, P]
+        _lib = lib
+        return lib
+
+
+def strerror(status: int) -> str:
+    return load().fp8l_strerror(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise Fp8LinearError(status, where)
+
+
+def _codes(t: torch.Tensor) -> torch.Tensor:
+    return t.view(torch.uint8) if t.dtype == torch.float8_e4m3fn else t
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not isinstance(t, torch.Tensor) or not t.is_cuda):
+            raise TypeError("expected CUDA tensors")
+        if t is not None and not t.is_contiguous():
+            raise ValueError("expected contiguous tensors")
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def fp8l_workspace_bytes() -> int:
+    return int(load().fp8l_workspace_bytes())
+
+
+def workspace(device=None) -> torch.Tensor:
+    """A zero-filled workspace for `device`, allocated once and reused."""
+    device = torch.device("cuda", torch.cuda.current_device() if device is None
+                          else torch.device(device).index or 0)
+    ws = _workspaces.get(device)
+    if ws is None:
+        ws = torch.zeros(fp8l_workspace_bytes(), dtype=torch.uint8, device=device)
+        _workspaces[device] = ws
+    return ws
+
+
+def fp8l_read_status(ws: torch.Tensor) -> int:
+    with torch.cuda.device(ws.device):
+        return int(load().fp8l_read_status(ws.data_ptr(), _stream(ws.device)))
+
+
+def fp8_quant_per_tensor(x: torch.Tensor, q: torch.Tensor | None = None,
+                         scale: torch.Tensor | None = None, dynamic: bool = True,
+                         ws: torch.Tensor | None = None):
+    """Per-tensor E4M3 quantization of x.  Returns (q uint8, scale float32[1]).
+    dynamic=False reads the given `scale` (static input scale)."""
+    _need_cuda(x, q, scale, ws)
+    if q is None:
+        q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if scale is None:
+        if not dynamic:
+            raise ValueError("static quantization needs a scale tensor")
+        scale = torch.empty(1, dtype=torch.float32, device=x.device)
+    if dynamic and ws is None:
+        ws = workspace(x.device)
+    rows = x.shape[0] if x.dim() > 1 else 1
+    cols = x.numel() // rows if rows else 0
+    with torch.cuda.device(x.device):
+        st = load().fp8_quant_per_tensor(
+            x.data_ptr(), _DTYPE_CODE[x.dtype], rows, cols, _codes(q).data_ptr(),
+            scale.data_ptr(), 1 if dynamic else 0, ws.data_ptr() if ws is not None else None,
+            _stream(x.device))
+    _check(st, "fp8_quant_per_tensor")
+    return q, scale
+
+
+def fp8_quant_per_row(x: torch.Tensor, q: torch.Tensor | None = None,
+                      row_scale: torch.Tensor | None = None):
+    """One dynamic scale per row of a 2-D tensor.  Returns (q uint8, scales float32[rows])."""
+    _need_cuda(x, q, row_scale)
+    if x.dim() != 2:
+        raise ValueError("expected a 2-D tensor")
+    rows, cols = x.shape
+    if q is None:
+        q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    if row_scale is None:
+        row_scale = torch.empty(rows, dtype=torch.float32, device=x.device)
+    with torch.cuda.device(x.device):
+        st = load().fp8_quant_per_row(x.data_ptr(), _DTYPE_CODE[x.dtype], rows, cols,
+                                      _codes(q).data_ptr(), row_scale.data_ptr(),
+                                      _stream(x.device))
+    _check(st, "fp8_quant_per_row")
+    return q, row_scale
+
+
+def fp8_scaled_mm(a: torch.Tensor, w: torch.Tensor, a_scale: torch.Tensor,
+                  w_scale: torch.Tensor, out_dtype=torch.bfloat16,
+                  out_scale: torch.Tensor | None = None, y: torch.Tensor | None = None,
+                  ws: torch.Tensor | None = None) -> torch.Tensor:
+    """W8A8 product of E4M3 a [M, K] and w [N, K] with per-tensor a_scale and a
+    per-tensor ([1]) or per-channel ([N]) w_scale.  out_dtype bf16 / fp16, or
+    uint8 (E4M3 codes, needs out_scale)."""
+    _need_cuda(a, w, a_scale, w_scale, out_scale, y, ws)
+    a, w = _codes(a), _codes(w)
+    M, K = a.shape
+    N = w.shape[0]
+    if w.shape[1] != K:
+        raise ValueError("inner dimensions differ")
+    if out_dtype == torch.float8_e4m3fn:
+        out_dtype = torch.uint8
+    code = _DTYPE_CODE[out_dtype]
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=a.device)
+    if ws is None:
+        ws = workspace(a.device)
+    per_channel = 1 if w_scale.numel() == N and N != 1 else 0
+    if w_scale.numel() not in (1, N):
+        raise ValueError("w_scale must have 1 or N entries")
+    with torch.cuda.device(a.device):
+        st = load().fp8_scaled_mm(
+            a.data_ptr(), w.data_ptr(), M, N, K, a_scale.data_ptr(), w_scale.data_ptr(),
+            per_channel, out_scale.data_ptr() if out_scale is not None else None,
+            _codes(y).data_ptr(), code, ws.data_ptr(), _stream(a.device))
+    _check(st, "fp8_scaled_mm")
+    return y
+
+
+def fp8_w8a16_mm(x: torch.Tensor, w: torch.Tensor, w_scale: torch.Tensor,
+                 y: torch.Tensor | None = None) -> torch.Tensor:
+    """Weight-only product: fp16/bf16 x [M, K] times E4M3 w [N, K] with
+    per-channel w_scale [N]; the output has x's dtype."""
+    _need_cuda(x, w, w_scale, y)
+    w = _codes(w)
+    M, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K or w_scale.numel() != N:
+        raise ValueError("shape mismatch")
+    if y is None:
+        y = torch.empty((M, N), dtype=x.dtype, device=x.device)
+    with torch.cuda.device(x.device):
+        st = load().fp8_w8a16_mm(x.data_ptr(), _DTYPE_CODE[x.dtype], w.data_ptr(),
+                                 w_scale.data_ptr(), M, N, K, y.data_ptr(), _stream(x.device))
+    _check(st, "fp8_w8a16_mm")
+    return y

@@ -1,0 +1,73 @@
+// Shared host and device helpers of the FP8 linear library (sm_103a only).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fp8linear.h"
+
+namespace fp8l {
+
+// ---------------------------------------------------------------------------
+// Workspace layout (fp8l_workspace_bytes bytes, zero-filled by the caller once)
+//   [0, 4)                   uint32 status word (bit flags below)
+//   [256, 256 + 4*kMaxParts) float per-block partial maxima of the quantizer
+constexpr size_t kStatusOffset = 0;
+constexpr size_t kPartialsOffset = 256;
+constexpr int kMaxPartials = 2048;
+constexpr size_t kWorkspaceBytes = kPartialsOffset + sizeof(float) * kMaxPartials;
+
+constexpr unsigned kStatusTimeout = 1u;  // a bounded device-side wait gave up
+
+// Largest magnitude of OCP E4M3.
+constexpr float kE4M3Max = 448.0f;
+
+// ---------------------------------------------------------------------------
+// host helpers
+
+inline bool aligned16(const void *p) {
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline unsigned *status_word(void *workspace) {
+    return reinterpret_cast<unsigned *>(static_cast<char *>(workspace) + kStatusOffset);
+}
+
+inline float *partials(void *workspace) {
+    return reinterpret_cast<float *>(static_cast<char *>(workspace) + kPartialsOffset);
+}
+
+// FP8L_OK when the current device is compute capability 10.3; caches the
+// answer and the SM count per device ordinal.
+int check_device(int *sm_count_out);
+
+// FP8L_ECUDA if the last launch failed, else FP8L_OK.
+inline int launch_status() {
+    return cudaGetLastError() == cudaSuccess ? FP8L_OK : FP8L_ECUDA;
+}
+
+// Launchers shared between translation units.
+int launch_skinny_e4m3(const uint8_t *a, const uint8_t *w, int M, int N, int K,
+                       const float *a_scale, const float *w_scale, int w_per_channel,
+                       const float *out_scale, void *y, int out_dtype, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// device helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte load that bypasses L1 (streamed weights).
+__device__ __forceinline__ uint4 ld_stream16(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+}  // namespace fp8l

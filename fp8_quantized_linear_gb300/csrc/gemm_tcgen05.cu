@@ -1,0 +1,522 @@
+// W8A8 scaled product on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// ("[Kernel][FP8] Initial support with dynamic per-tensor scaling": the
+// forward pass is torch._scaled_mm of the E4M3 activations and weights with
+// their scales; "Marlin fp8": per-output-channel weight scales; "RFC: FP8
+// Quantization Schema in vLLM": output_scale for an E4M3 result.)
+//
+//   y[m, n] = cast( sum_k dec(a[m,k]) dec(w[n,k]) * a_scale * w_scale(n) )
+//
+// Structure (one persistent CTA per SM, 192 threads):
+//   warp 0      TMA producer: 128x128 A tile and 256x128 W tile per k-block
+//               (E4M3 bytes, 128-byte swizzle) into a STAGES-deep ring of
+//               shared-memory stages guarded by full/empty mbarriers.
+//   warp 1      owns the TMEM allocation (2 x 256 fp32 columns: a double
+//               buffered 128x256 accumulator) and one lane issues
+//               tcgen05.mma.cta_group::1.kind::f8f6f4 (M=128, N=256, K=32),
+//               four per k-block; tcgen05.commit frees a stage when its
+//               MMAs retire and publishes a finished accumulator.
+//   warps 2-5   epilogue: tcgen05.ld of their 32 TMEM lanes (= tile rows),
+//               scale by a_scale * w_scale(n), round to bf16/fp16 or divide
+//               by output_scale and cast to E4M3, 16-byte stores.  With two
+//               accumulators the epilogue of tile i overlaps the MMAs of
+//               tile i+1.
+// Tiles are visited M-block fastest, so the CTAs working at one time share a
+// few W column blocks and all of A in L2.  Out-of-range rows / K columns of
+// a tile are zero-filled by TMA and masked in the epilogue.
+// Every mbarrier wait is bounded: on time-out the CTA raises an abort flag,
+// records FP8L_ETIMEOUT in the workspace status word, lets the other roles
+// drop out, waits (bounded) for its own copies and MMAs, frees TMEM, returns.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+
+#include "common.cuh"
+
+namespace fp8l {
+namespace {
+
+constexpr int BM = 128;           // tile rows (tokens)      = MMA M
+constexpr int BN = 256;           // tile columns (channels) = MMA N
+constexpr int BK = 128;           // k-block, bytes = E4M3 elements = swizzle span
+constexpr int UMMA_K = 32;        // K of one kind::f8f6f4 MMA
+constexpr int STAGES = 4;
+constexpr int kABytes = BM * BK;  // 16 KB
+constexpr int kBBytes = BN * BK;  // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kTmemCols = 2 * BN;  // two accumulators
+constexpr int kThreads = 192;
+constexpr int kEpiWarps = 4;
+constexpr int kNumBarriers = 2 * STAGES + 2 + 2 + 1;
+constexpr size_t kSmemBytes = 1024 + size_t(STAGES) * kStageBytes + kNumBarriers * 8 + 16;
+
+// ~2 s at 2 GHz: a healthy wait in this kernel is microseconds
+constexpr long long kWaitCycles = 4LL << 30;
+
+struct GemmParams {
+    int M, N, K;
+    int num_m_blocks, num_n_blocks, num_k_blocks;
+    const float *a_scale;
+    const float *w_scale;
+    int w_per_channel;
+    const float *out_scale;
+    void *y;
+    int out_dtype;
+    unsigned *status;
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// Bounded wait for the phase of parity `parity`.  Gives up when another
+// role raised the abort flag, or after kWaitCycles (then raises it and
+// records the time-out).
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                       unsigned *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0u) {
+            if (*abort_flag) return false;
+            if (clock64() - t0 > kWaitCycles) {
+                *abort_flag = 1;
+                atomicOr(status, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait used while tearing down: ignores the abort flag.
+__device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, unsigned *status) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kWaitCycles) {
+            atomicOr(status, kStatusTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format) of a K-major operand tile
+// laid out by TMA with the 128-byte swizzle: 128-byte rows, 8-row groups
+// 1024 bytes apart (stride byte offset), version field 1, swizzle mode 2.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+           (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) |
+           (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+
+// Instruction descriptor, kind::f8f6f4: D f32 (bits 4-5 = 1), A and B E4M3
+// (format 0, bits 7-9 and 10-12), both K-major (bits 15, 16 = 0),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- epilogue
+
+__device__ __forceinline__ uint32_t pack_out16(float a, float b, int out_dtype) {
+    if (out_dtype == FP8L_BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+    return static_cast<uint32_t>(
+        __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+
+// Scales and stores 32 accumulator columns [n0, n0+32) of row m.
+__device__ __forceinline__ void store_row_chunk(const GemmParams &p, const uint32_t (&r)[32],
+                                                int m, int n0, float sa_sw) {
+    const bool full32 = n0 + 32 <= p.N;  // N % 16 == 0: else exactly 16 columns remain
+    float v[32];
+    if (p.w_per_channel) {
+        const float sa = __ldg(p.a_scale);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float sw = (j < 16 || full32) ? __ldg(p.w_scale + n0 + j) : 0.0f;
+            v[j] = __uint_as_float(r[j]) * (sa * sw);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * sa_sw;
+    }
+    if (p.out_dtype == FP8L_E4M3) {
+        const float os = __ldg(p.out_scale);
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t lo = e4m3x2(__fdiv_rn(v[4 * i], os), __fdiv_rn(v[4 * i + 1], os));
+            const uint32_t hi = e4m3x2(__fdiv_rn(v[4 * i + 2], os), __fdiv_rn(v[4 * i + 3], os));
+            w[i] = lo | (hi << 16);
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.y) +
+                                               static_cast<size_t>(m) * p.N + n0);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        if (full32) dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    } else {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = pack_out16(v[2 * i], v[2 * i + 1], p.out_dtype);
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.y) +
+                                               static_cast<size_t>(m) * p.N + n0);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        if (full32) {
+            dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+            dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- kernel
+
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
+                const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;  // swizzle atoms need 1024-byte alignment
+    uint8_t *gbase = smem_raw + (sbase - raw);
+    const uint32_t bar0 = sbase + STAGES * kStageBytes;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + STAGES * kStageBytes + kNumBarriers * 8);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), kEpiWarps);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int num_tiles = p.num_m_blocks * p.num_n_blocks;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued = 0, issued_parity = 0;  // per stage: load in flight, its parity
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                const int mb = tile % p.num_m_blocks;
+                const int nb = tile / p.num_m_blocks;
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = sbase + stage * kStageBytes;
+                    mbar_expect_tx(full_bar(stage), kStageBytes);
+                    tma_load_2d(sa, &tmap_a, kb * BK, mb * BM, full_bar(stage));
+                    tma_load_2d(sa + kABytes, &tmap_b, kb * BK, nb * BN, full_bar(stage));
+                    issued |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // every load this thread issued must land before the CTA exits
+            for (int s = 0; s < STAGES; ++s)
+                if (issued & (1u << s)) mbar_wait_drain(full_bar(s), (issued_parity >> s) & 1u, p.status);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = sbase + stage * kStageBytes;
+                    const uint32_t sb = sa + kABytes;
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; ++k)
+                        mma_f8(d_tmem, sw128_desc(sa + k * UMMA_K), sw128_desc(sb + k * UMMA_K),
+                               (kb | k) != 0 ? 1u : 0u);
+                    mma_commit(empty_bar(stage));  // stage reusable once these MMAs retire
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(tfull_bar(acc));  // accumulator ready once all MMAs retire
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            // all MMAs of this CTA retire before TMEM is freed
+            mma_commit(done_bar);
+            mbar_wait_drain(done_bar, 0, p.status);
+        }
+        __syncwarp();
+    } else {
+        const int quarter = warp & 3;  // TMEM lanes this warp may read: 32*quarter ..
+        const int row = quarter * 32 + lane;
+        float sa_sw = 0.0f;
+        if (!p.w_per_channel) sa_sw = __ldg(p.a_scale) * __ldg(p.w_scale);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            const int mb = tile % p.num_m_blocks;
+            const int nb = tile / p.num_m_blocks;
+            if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status)) break;
+            tc_fence_after();
+            const int m = mb * BM + row;
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(taddr + static_cast<uint32_t>(c * 32), r);
+                const int n0 = nb * BN + c * 32;
+                if (m < p.M && n0 < p.N) store_row_chunk(p, r, m, n0, sa_sw);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> fn{nullptr};
+    PFN_cuTensorMapEncodeTiled_v12000 f = fn.load(std::memory_order_acquire);
+    if (f == nullptr) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        f = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        fn.store(f, std::memory_order_release);
+    }
+    return f;
+}
+
+// 2-D map over a row-major [rows, K] uint8 matrix, box BK x box_rows, 128B swizzle
+int make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (enc == nullptr) return FP8L_ECUDA;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8L_OK : FP8L_ECUDA;
+}
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_smem_set[kMaxDevices];
+
+int ensure_smem_attr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP8L_ECUDA;
+    if (g_smem_set[dev].load(std::memory_order_acquire)) return FP8L_OK;
+    if (cudaFuncSetAttribute(gemm_f8_tcgen05, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes)) != cudaSuccess)
+        return FP8L_ECUDA;
+    g_smem_set[dev].store(1, std::memory_order_release);
+    return FP8L_OK;
+}
+
+int launch_tcgen05(const uint8_t *a, const uint8_t *w, int M, int N, int K, const float *a_scale,
+                   const float *w_scale, int w_per_channel, const float *out_scale, void *y,
+                   int out_dtype, unsigned *status, int sms, cudaStream_t stream) {
+    CUtensorMap ma, mb;
+    if (make_map(&ma, a, M, K, BM) != FP8L_OK) return FP8L_ECUDA;
+    if (make_map(&mb, w, N, K, BN) != FP8L_OK) return FP8L_ECUDA;
+    if (ensure_smem_attr() != FP8L_OK) return FP8L_ECUDA;
+    GemmParams p;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.num_m_blocks = (M + BM - 1) / BM;
+    p.num_n_blocks = (N + BN - 1) / BN;
+    p.num_k_blocks = (K + BK - 1) / BK;
+    p.a_scale = a_scale;
+    p.w_scale = w_scale;
+    p.w_per_channel = w_per_channel;
+    p.out_scale = out_scale;
+    p.y = y;
+    p.out_dtype = out_dtype;
+    p.status = status;
+    const int64_t tiles = int64_t(p.num_m_blocks) * p.num_n_blocks;
+    const int grid = static_cast<int>(tiles < sms ? tiles : sms);
+    gemm_f8_tcgen05<<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, p);
+    return launch_status();
+}
+
+}  // namespace
+}  // namespace fp8l
+
+extern "C" int fp8_scaled_mm(const uint8_t *a, const uint8_t *w, int64_t M, int64_t N, int64_t K,
+                             const float *a_scale, const float *w_scale, int w_per_channel,
+                             const float *out_scale, void *y, int out_dtype, void *workspace,
+                             void *stream) {
+    using namespace fp8l;
+    if (out_dtype != FP8L_F16 && out_dtype != FP8L_BF16 && out_dtype != FP8L_E4M3)
+        return FP8L_EINVAL;
+    if (a_scale == nullptr || w_scale == nullptr || workspace == nullptr || w == nullptr)
+        return FP8L_EINVAL;
+    if (out_dtype == FP8L_E4M3 && out_scale == nullptr) return FP8L_EINVAL;
+    if (M < 0 || M > 0x7FFFFFFF || N <= 0 || K <= 0 || N > (1 << 20) || K > (1 << 20) ||
+        N % 16 != 0 || K % 16 != 0)
+        return FP8L_ESHAPE;
+    if (M > 0 && (a == nullptr || y == nullptr)) return FP8L_EINVAL;
+    auto misaligned4 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) != 0; };
+    if (!aligned16(w) || !aligned16(workspace) || (M > 0 && (!aligned16(a) || !aligned16(y))) ||
+        misaligned4(a_scale) || misaligned4(w_scale) ||
+        (out_dtype == FP8L_E4M3 && misaligned4(out_scale)))
+        return FP8L_EALIGN;
+    int sms = 0;
+    int st = check_device(&sms);
+    if (st != FP8L_OK) return st;
+    if (M == 0) return FP8L_OK;
+    cudaStream_t s = as_stream(stream);
+    const int pc = w_per_channel ? 1 : 0;
+    if (M <= 16)
+        return launch_skinny_e4m3(a, w, static_cast<int>(M), static_cast<int>(N),
+                                  static_cast<int>(K), a_scale, w_scale, pc, out_scale, y,
+                                  out_dtype, s);
+    return launch_tcgen05(a, w, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                          a_scale, w_scale, pc, out_scale, y, out_dtype, status_word(workspace),
+                          sms, s);
+}

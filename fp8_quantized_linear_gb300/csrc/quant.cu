@@ -1,0 +1,329 @@
+// Per-tensor and per-row quantization to OCP E4M3.
+//
+// Per-tensor, dynamic ("[Kernel][FP8] Initial support with dynamic per-tensor
+// scaling", Algorithm): two bandwidth-bound launches.
+//   1. absmax_kernel: every thread streams 16-element chunks with 16-byte
+//      loads and keeps the running maximum of the magnitude BITS (sign bit
+//      cleared; for finite IEEE values, a larger magnitude has larger unsigned
+//      bits, so the maximum is exact and needs no float compare).  Warp
+//      reduction with redux.sync, block reduction in shared memory, one
+//      partial per block into the workspace.
+//   2. cast_kernel: every block reduces the partials (a few hundred floats,
+//      L2 resident), forms s = amax / 448 (IEEE division, 1 when zero), and
+//      casts its chunks: q = E4M3_satRNE(x / s) with an IEEE division per
+//      element and the hardware saturating RNE conversion.  Block 0 writes s.
+//   The second pass re-reads X; X up to ~100 MB is still in the 126 MB L2.
+// Static mode ("RFC: FP8 Quantization Schema in vLLM", input scales) runs
+// only the cast kernel with s read from device memory.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+
+namespace fp8l {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kChunk = 16;  // elements per chunk (one 16-byte store of codes)
+
+// uint4 words per chunk = bytes per element (16 elements)
+template <int DT> struct Elt;
+template <> struct Elt<FP8L_F16> { static constexpr int kBytes = 2; };
+template <> struct Elt<FP8L_BF16> { static constexpr int kBytes = 2; };
+template <> struct Elt<FP8L_F32> { static constexpr int kBytes = 4; };
+
+template <int DT>
+__device__ __forceinline__ void load_chunk(const uint4 *__restrict__ base, int64_t c,
+                                           uint4 (&v)[Elt<DT>::kBytes]) {
+#pragma unroll
+    for (int i = 0; i < Elt<DT>::kBytes; ++i) v[i] = __ldg(base + c * Elt<DT>::kBytes + i);
+}
+
+// running max of magnitude bits; for 16-bit types two magnitudes per word
+template <int DT>
+__device__ __forceinline__ uint32_t chunk_mag_max(const uint4 (&v)[Elt<DT>::kBytes], uint32_t m) {
+#pragma unroll
+    for (int i = 0; i < Elt<DT>::kBytes; ++i) {
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if constexpr (DT == FP8L_F32)
+                m = max(m, w[j] & 0x7FFFFFFFu);
+            else
+                m = __vmaxu2(m, w[j] & 0x7FFF7FFFu);
+        }
+    }
+    return m;
+}
+
+// fold packed 16-bit maxima into one magnitude bit pattern
+template <int DT>
+__device__ __forceinline__ uint32_t fold_mag(uint32_t m) {
+    if constexpr (DT == FP8L_F32) return m;
+    return max(m & 0xFFFFu, m >> 16);
+}
+
+template <int DT>
+__device__ __forceinline__ float mag_bits_to_float(uint32_t m) {
+    if constexpr (DT == FP8L_F32) return __uint_as_float(m);
+    if constexpr (DT == FP8L_BF16) return __uint_as_float(m << 16);
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(m)));
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t scalar_mag_bits(const void *x, int64_t i) {
+    if constexpr (DT == FP8L_F32)
+        return __float_as_uint(static_cast<const float *>(x)[i]) & 0x7FFFFFFFu;
+    return static_cast<uint32_t>(static_cast<const unsigned short *>(x)[i]) & 0x7FFFu;
+}
+
+template <int DT>
+__device__ __forceinline__ float scalar_value(const void *x, int64_t i) {
+    if constexpr (DT == FP8L_F32) return static_cast<const float *>(x)[i];
+    if constexpr (DT == FP8L_BF16)
+        return __uint_as_float(static_cast<uint32_t>(static_cast<const unsigned short *>(x)[i]) << 16);
+    return __half2float(static_cast<const __half *>(x)[i]);
+}
+
+// the 16 values of a chunk as floats (exact widening)
+template <int DT>
+__device__ __forceinline__ void chunk_values(const uint4 (&v)[Elt<DT>::kBytes], float (&f)[kChunk]) {
+#pragma unroll
+    for (int i = 0; i < Elt<DT>::kBytes; ++i) {
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if constexpr (DT == FP8L_F32) {
+                f[i * 4 + j] = __uint_as_float(w[j]);
+            } else if constexpr (DT == FP8L_BF16) {
+                f[i * 8 + 2 * j] = __uint_as_float(w[j] << 16);
+                f[i * 8 + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+            } else {
+                __half2 h = *reinterpret_cast<const __half2 *>(&w[j]);
+                float2 p = __half22float2(h);
+                f[i * 8 + 2 * j] = p.x;
+                f[i * 8 + 2 * j + 1] = p.y;
+            }
+        }
+    }
+}
+
+// saturating round-to-nearest-even E4M3 codes of (a, b); a in the low byte
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+    return static_cast<uint32_t>(
+        __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+
+__device__ __forceinline__ uint8_t e4m3(float a) {
+    return static_cast<uint8_t>(__nv_cvt_float_to_fp8(a, __NV_SATFINITE, __NV_E4M3));
+}
+
+__device__ __forceinline__ uint4 quant_chunk(const float (&f)[kChunk], float s) {
+    uint32_t p[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        p[i] = e4m3x2(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
+    return make_uint4(p[0] | (p[1] << 16), p[2] | (p[3] << 16), p[4] | (p[5] << 16),
+                      p[6] | (p[7] << 16));
+}
+
+// maximum over the block; every thread gets the result
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t m, uint32_t *red) {
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t v = lane < (blockDim.x >> 5) ? red[lane] : 0u;
+        v = __reduce_max_sync(0xFFFFFFFFu, v);
+        if (lane == 0) red[32] = v;
+    }
+    __syncthreads();
+    return red[32];
+}
+
+__device__ __forceinline__ float scale_from_amax(float amax) {
+    float s = __fdiv_rn(amax, kE4M3Max);
+    return s == 0.0f ? 1.0f : s;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads)
+absmax_kernel(const void *__restrict__ x, int64_t numel, float *__restrict__ part) {
+    __shared__ uint32_t red[33];
+    const uint4 *xv = static_cast<const uint4 *>(x);
+    const int64_t n_chunks = numel / kChunk;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    int64_t c = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    uint32_t m = 0;
+    for (; c + stride < n_chunks; c += 2 * stride) {
+        uint4 v0[Elt<DT>::kBytes], v1[Elt<DT>::kBytes];
+        load_chunk<DT>(xv, c, v0);
+        load_chunk<DT>(xv, c + stride, v1);
+        m = chunk_mag_max<DT>(v0, m);
+        m = chunk_mag_max<DT>(v1, m);
+    }
+    if (c < n_chunks) {
+        uint4 v0[Elt<DT>::kBytes];
+        load_chunk<DT>(xv, c, v0);
+        m = chunk_mag_max<DT>(v0, m);
+    }
+    m = fold_mag<DT>(m);
+    const int64_t tail = numel - n_chunks * kChunk;
+    if (blockIdx.x == 0 && threadIdx.x < tail)
+        m = max(m, scalar_mag_bits<DT>(x, n_chunks * kChunk + threadIdx.x));
+    m = block_max_u32(m, red);
+    if (threadIdx.x == 0) part[blockIdx.x] = mag_bits_to_float<DT>(m);
+}
+
+template <int DT, bool kDynamic>
+__global__ void __launch_bounds__(kThreads)
+cast_kernel(const void *__restrict__ x, int64_t numel, uint8_t *__restrict__ q,
+            float *__restrict__ scale, const float *__restrict__ part, int n_part) {
+    __shared__ uint32_t red[33];
+    float s;
+    if constexpr (kDynamic) {
+        uint32_t m = 0;  // partials are non-negative floats: compare their bits
+        for (int i = threadIdx.x; i < n_part; i += kThreads) m = max(m, __float_as_uint(part[i]));
+        m = block_max_u32(m, red);
+        s = scale_from_amax(__uint_as_float(m));
+        if (blockIdx.x == 0 && threadIdx.x == 0) *scale = s;
+    } else {
+        s = __ldg(scale);
+    }
+    const uint4 *xv = static_cast<const uint4 *>(x);
+    uint4 *qv = reinterpret_cast<uint4 *>(q);
+    const int64_t n_chunks = numel / kChunk;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t c = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; c < n_chunks;
+         c += stride) {
+        uint4 v[Elt<DT>::kBytes];
+        float f[kChunk];
+        load_chunk<DT>(xv, c, v);
+        chunk_values<DT>(v, f);
+        qv[c] = quant_chunk(f, s);
+    }
+    const int64_t tail = numel - n_chunks * kChunk;
+    if (blockIdx.x == 0 && threadIdx.x < tail) {
+        const int64_t i = n_chunks * kChunk + threadIdx.x;
+        q[i] = e4m3(__fdiv_rn(scalar_value<DT>(x, i), s));
+    }
+}
+
+// one block per row; cols is a multiple of 16
+template <int DT>
+__global__ void __launch_bounds__(kThreads)
+row_quant_kernel(const void *__restrict__ x, int64_t cols, uint8_t *__restrict__ q,
+                 float *__restrict__ row_scale) {
+    __shared__ uint32_t red[33];
+    const int64_t r = blockIdx.x;
+    const int64_t n_chunks = cols / kChunk;
+    const uint4 *xv = reinterpret_cast<const uint4 *>(
+        static_cast<const char *>(x) + r * cols * Elt<DT>::kBytes);
+    uint4 *qv = reinterpret_cast<uint4 *>(q + r * cols);
+    uint32_t m = 0;
+    for (int64_t c = threadIdx.x; c < n_chunks; c += kThreads) {
+        uint4 v[Elt<DT>::kBytes];
+        load_chunk<DT>(xv, c, v);
+        m = chunk_mag_max<DT>(v, m);
+    }
+    m = block_max_u32(fold_mag<DT>(m), red);
+    const float s = scale_from_amax(mag_bits_to_float<DT>(m));
+    if (threadIdx.x == 0) row_scale[r] = s;
+    for (int64_t c = threadIdx.x; c < n_chunks; c += kThreads) {
+        uint4 v[Elt<DT>::kBytes];
+        float f[kChunk];
+        load_chunk<DT>(xv, c, v);
+        chunk_values<DT>(v, f);
+        qv[c] = quant_chunk(f, s);
+    }
+}
+
+constexpr int64_t kMaxNumel = int64_t(1) << 40;
+
+template <int DT>
+int run_per_tensor(const void *x, int64_t numel, uint8_t *q, float *scale, bool dynamic,
+                   void *workspace, cudaStream_t stream, int sms) {
+    const int64_t n_chunks = numel / kChunk;
+    const int64_t cast_blocks_needed = (n_chunks + kThreads - 1) / kThreads;
+    const int cast_blocks = static_cast<int>(
+        cast_blocks_needed < 1 ? 1 : (cast_blocks_needed < int64_t(sms) * 8 ? cast_blocks_needed
+                                                                               : int64_t(sms) * 8));
+    if (!dynamic) {
+        if (numel == 0) return FP8L_OK;
+        cast_kernel<DT, false><<<cast_blocks, kThreads, 0, stream>>>(x, numel, q, scale, nullptr, 0);
+        return launch_status();
+    }
+    float *part = partials(workspace);
+    int n_part = 0;
+    if (numel > 0) {
+        const int64_t want = (n_chunks + 2 * kThreads - 1) / (2 * kThreads);
+        int64_t blocks = want < 1 ? 1 : want;
+        if (blocks > int64_t(sms) * 8) blocks = int64_t(sms) * 8;
+        if (blocks > kMaxPartials) blocks = kMaxPartials;
+        n_part = static_cast<int>(blocks);
+        absmax_kernel<DT><<<n_part, kThreads, 0, stream>>>(x, numel, part);
+        if (launch_status() != FP8L_OK) return FP8L_ECUDA;
+    }
+    cast_kernel<DT, true><<<cast_blocks, kThreads, 0, stream>>>(x, numel, q, scale, part, n_part);
+    return launch_status();
+}
+
+template <int DT>
+int run_per_row(const void *x, int64_t rows, int64_t cols, uint8_t *q, float *row_scale,
+                cudaStream_t stream) {
+    if (rows == 0) return FP8L_OK;
+    // an empty row (cols == 0) gets amax 0, hence scale 1
+    row_quant_kernel<DT><<<static_cast<unsigned>(rows), kThreads, 0, stream>>>(x, cols, q, row_scale);
+    return launch_status();
+}
+
+bool valid_in_dtype(int dt) { return dt == FP8L_F16 || dt == FP8L_BF16 || dt == FP8L_F32; }
+
+}  // namespace
+}  // namespace fp8l
+
+extern "C" int fp8_quant_per_tensor(const void *x, int x_dtype, int64_t rows, int64_t cols,
+                                    uint8_t *q, float *scale, int dynamic, void *workspace,
+                                    void *stream) {
+    using namespace fp8l;
+    if (!valid_in_dtype(x_dtype) || scale == nullptr) return FP8L_EINVAL;
+    if (rows < 0 || cols < 0) return FP8L_ESHAPE;
+    if (cols != 0 && rows > kMaxNumel / cols) return FP8L_ESHAPE;
+    const int64_t numel = rows * cols;
+    if (numel > 0 && (x == nullptr || q == nullptr)) return FP8L_EINVAL;
+    if (dynamic && workspace == nullptr) return FP8L_EINVAL;
+    if ((numel > 0 && (!aligned16(x) || !aligned16(q))) || !aligned16(workspace))
+        return FP8L_EALIGN;
+    if ((reinterpret_cast<uintptr_t>(scale) & 3u) != 0) return FP8L_EALIGN;
+    int sms = 0;
+    int st = check_device(&sms);
+    if (st != FP8L_OK) return st;
+    cudaStream_t s = as_stream(stream);
+    switch (x_dtype) {
+        case FP8L_F16: return run_per_tensor<FP8L_F16>(x, numel, q, scale, dynamic != 0, workspace, s, sms);
+        case FP8L_BF16: return run_per_tensor<FP8L_BF16>(x, numel, q, scale, dynamic != 0, workspace, s, sms);
+        default: return run_per_tensor<FP8L_F32>(x, numel, q, scale, dynamic != 0, workspace, s, sms);
+    }
+}
+
+extern "C" int fp8_quant_per_row(const void *x, int x_dtype, int64_t rows, int64_t cols,
+                                 uint8_t *q, float *row_scale, void *stream) {
+    using namespace fp8l;
+    if (!valid_in_dtype(x_dtype)) return FP8L_EINVAL;
+    if (rows < 0 || cols < 0 || rows > 0x7FFFFFFF || cols > (int64_t(1) << 20) || cols % 16 != 0)
+        return FP8L_ESHAPE;
+    if (rows > 0 && (x == nullptr || q == nullptr || row_scale == nullptr)) return FP8L_EINVAL;
+    if (rows > 0 && (!aligned16(x) || !aligned16(q) ||
+                     (reinterpret_cast<uintptr_t>(row_scale) & 3u) != 0))
+        return FP8L_EALIGN;
+    int st = check_device(nullptr);
+    if (st != FP8L_OK) return st;
+    cudaStream_t s = as_stream(stream);
+    switch (x_dtype) {
+        case FP8L_F16: return run_per_row<FP8L_F16>(x, rows, cols, q, row_scale, s);
+        case FP8L_BF16: return run_per_row<FP8L_BF16>(x, rows, cols, q, row_scale, s);
+        default: return run_per_row<FP8L_F32>(x, rows, cols, q, row_scale, s);
+    }
+}

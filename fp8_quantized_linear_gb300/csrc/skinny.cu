@@ -1,0 +1,267 @@
+// Weight-streaming products for small token counts (M <= 16 per launch row):
+//   * W8A16 ("Marlin fp8"): fp16/bf16 activations x E4M3 weights with one
+//     scale per output channel;
+//   * W8A8 small-M branch of the scaled product ("[Kernel][FP8] Initial
+//     support ...", the M = 1..16 rows of the microbenchmark list, where the
+//     product is bound by reading the weights).
+//
+// Design (HBM-bound: the weights are read once, every other operand is small)
+//   * One CTA owns 16 output channels (rows of W) and one group of up to 16
+//     tokens; its WARPS warps split K in 64-element chunks (chunk c goes to
+//     warp c mod WARPS), then add their partial tiles in shared memory.
+//   * Lane (g, t) = (lane / 4, lane % 4) reads 16 contiguous weight bytes
+//     of channel rows g and g + 8 per chunk with one streaming 16-byte load
+//     each (a warp load covers 8 rows x 64 contiguous bytes).  The K order
+//     inside a chunk is permuted identically for weights and activations, so
+//     every lane's 16 bytes feed its own tensor-core fragment slots and no
+//     shuffle is needed; a sum over k does not depend on the order of k.
+//   * Tensor cores (mma.sync): weights are the 16-row A operand, tokens the
+//     8-column B operand (two B tiles for 9..16 tokens), fp32 accumulation.
+//     W8A16 decodes E4M3 to f16 with the hardware conversion (exact); for
+//     bf16 activations the f16 values are widened to bf16 (exact).  W8A8 uses
+//     the E4M3 x E4M3 tensor-core form directly (m16n8k32).
+//   * Epilogue: per-channel (or per-tensor) scale, activation scale, then an
+//     f16/bf16 round-to-nearest store or an E4M3 re-quantization through
+//     output_scale, one output element per thread with coalesced stores.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+
+namespace fp8l {
+namespace {
+
+enum XKind { kXF16 = 0, kXBF16 = 1, kXE4M3 = 2 };
+
+struct SkinnyArgs {
+    const uint8_t *w;  // [N, K] E4M3
+    const void *x;     // [M, K] f16 / bf16 / E4M3
+    int M, N, K;
+    const float *a_scale;    // E4M3 activations only
+    const float *w_scale;    // [1] or [N]
+    int w_per_channel;
+    const float *out_scale;  // E4M3 output only
+    void *y;                 // [M, N]
+    int out_dtype;
+};
+
+__device__ __forceinline__ uint32_t dec_f16x2(uint32_t pair) {
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(pair & 0xFFFFu),
+                                               __NV_E4M3);
+    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+__device__ __forceinline__ uint32_t dec_bf16x2(uint32_t pair) {
+    uint32_t h = dec_f16x2(pair);
+    float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+    __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+    return *reinterpret_cast<const uint32_t *>(&b);
+}
+
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_e4m3(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Bytes of one token's activations per 64-element chunk: 128 (16-bit) or 64.
+template <int XK> struct XBytes { static constexpr int kPerLane = (XK == kXE4M3) ? 16 : 32; };
+
+template <int XK, int NT, int WARPS, int UNROLL>
+__global__ void __launch_bounds__(WARPS * 32)
+skinny_kernel(const SkinnyArgs args) {
+    constexpr int kXWords = XBytes<XK>::kPerLane / 4;  // 32-bit words per lane per token
+    __shared__ float red[WARPS][NT][4][32];
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int g = lane >> 2;
+    const int t4 = lane & 3;
+    const int n0 = blockIdx.x * 16;
+    const int m0 = blockIdx.y * 16;
+    const int K = args.K;
+    const int M = args.M;
+    const int nchunks = (K + 63) >> 6;
+
+    const uint8_t *w_g = args.w + static_cast<size_t>(n0 + g) * K + 16 * t4;
+    const uint8_t *w_g8 = w_g + static_cast<size_t>(8) * K;
+    const char *xbase = static_cast<const char *>(args.x);
+    constexpr int kXElt = (XK == kXE4M3) ? 1 : 2;
+
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[nt][r] = 0.0f;
+
+    for (int c0 = warp; c0 < nchunks; c0 += WARPS * UNROLL) {
+        uint4 wa[UNROLL], wb[UNROLL];
+        uint32_t xw[UNROLL][NT][kXWords];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int c = c0 + u * WARPS;
+            const int kk = c * 64 + 16 * t4;  // first k of this lane's 16
+            const bool kin = (c < nchunks) && (kk < K);
+            wa[u] = kin ? ld_stream16(w_g + static_cast<size_t>(c) * 64) : make_uint4(0, 0, 0, 0);
+            wb[u] = kin ? ld_stream16(w_g8 + static_cast<size_t>(c) * 64) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int m = m0 + g + 8 * nt;
+                const bool in = kin && (m < M);
+                const uint4 *xp = reinterpret_cast<const uint4 *>(
+                    xbase + (static_cast<size_t>(m) * K + kk) * kXElt);
+#pragma unroll
+                for (int v = 0; v < kXWords / 4; ++v) {
+                    uint4 t = in ? __ldg(xp + v) : make_uint4(0, 0, 0, 0);
+                    xw[u][nt][4 * v + 0] = t.x;
+                    xw[u][nt][4 * v + 1] = t.y;
+                    xw[u][nt][4 * v + 2] = t.z;
+                    xw[u][nt][4 * v + 3] = t.w;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const uint32_t ra[4] = {wa[u].x, wa[u].y, wa[u].z, wa[u].w};  // row g
+            const uint32_t rb[4] = {wb[u].x, wb[u].y, wb[u].z, wb[u].w};  // row g + 8
+            if constexpr (XK == kXE4M3) {
+                // two k32 steps; step j uses bytes 8j..8j+7 of the lane's 16
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma_e4m3(acc[nt], ra[2 * j], rb[2 * j], ra[2 * j + 1], rb[2 * j + 1],
+                                 xw[u][nt][2 * j], xw[u][nt][2 * j + 1]);
+                }
+            } else {
+                // four k16 steps; step j uses bytes 4j..4j+3 of the lane's 16:
+                // (4j, 4j+1) fill the low-k slots, (4j+2, 4j+3) the high-k slots
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t a0, a1, a2, a3;
+                    if constexpr (XK == kXF16) {
+                        a0 = dec_f16x2(ra[j]);
+                        a1 = dec_f16x2(rb[j]);
+                        a2 = dec_f16x2(ra[j] >> 16);
+                        a3 = dec_f16x2(rb[j] >> 16);
+                    } else {
+                        a0 = dec_bf16x2(ra[j]);
+                        a1 = dec_bf16x2(rb[j]);
+                        a2 = dec_bf16x2(ra[j] >> 16);
+                        a3 = dec_bf16x2(rb[j] >> 16);
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        if constexpr (XK == kXF16)
+                            mma_f16(acc[nt], a0, a1, a2, a3, xw[u][nt][2 * j], xw[u][nt][2 * j + 1]);
+                        else
+                            mma_bf16(acc[nt], a0, a1, a2, a3, xw[u][nt][2 * j], xw[u][nt][2 * j + 1]);
+                    }
+                }
+            }
+        }
+    }
+
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) red[warp][nt][r][lane] = acc[nt][r];
+    __syncthreads();
+
+    // one (token, channel) output per thread: channel fastest for coalescing
+    for (int o = threadIdx.x; o < 16 * 8 * NT; o += WARPS * 32) {
+        const int ch = o & 15;
+        const int tk = o >> 4;  // token within the group, 0 .. 8*NT-1
+        const int m = m0 + tk;
+        if (m >= M) continue;
+        const int nt = tk >> 3;
+        const int col = tk & 7;
+        const int lane_src = ((ch & 7) << 2) | (col >> 1);
+        const int r = ((ch >> 3) << 1) | (col & 1);
+        float sum = 0.0f;
+#pragma unroll
+        for (int wi = 0; wi < WARPS; ++wi) sum += red[wi][nt][r][lane_src];
+        const int n = n0 + ch;
+        float sc = args.w_per_channel ? __ldg(args.w_scale + n) : __ldg(args.w_scale);
+        if constexpr (XK == kXE4M3) sc *= __ldg(args.a_scale);
+        const float v = sum * sc;
+        const size_t yi = static_cast<size_t>(m) * args.N + n;
+        if (args.out_dtype == FP8L_F16) {
+            static_cast<__half *>(args.y)[yi] = __float2half_rn(v);
+        } else if (args.out_dtype == FP8L_BF16) {
+            static_cast<__nv_bfloat16 *>(args.y)[yi] = __float2bfloat16_rn(v);
+        } else {
+            const float t = __fdiv_rn(v, __ldg(args.out_scale));
+            static_cast<uint8_t *>(args.y)[yi] = static_cast<uint8_t>(
+                __nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3));
+        }
+    }
+}
+
+constexpr int kWarps = 8;
+constexpr int kUnroll = 4;
+
+template <int XK>
+int launch(const SkinnyArgs &a, cudaStream_t stream) {
+    if (a.M == 0) return FP8L_OK;
+    const dim3 grid(static_cast<unsigned>(a.N / 16), static_cast<unsigned>((a.M + 15) / 16));
+    const int tokens_in_group = a.M < 16 ? a.M : 16;
+    if (tokens_in_group <= 8)
+        skinny_kernel<XK, 1, kWarps, kUnroll><<<grid, kWarps * 32, 0, stream>>>(a);
+    else
+        skinny_kernel<XK, 2, kWarps, kUnroll><<<grid, kWarps * 32, 0, stream>>>(a);
+    return launch_status();
+}
+
+}  // namespace
+
+int launch_skinny_e4m3(const uint8_t *a, const uint8_t *w, int M, int N, int K,
+                       const float *a_scale, const float *w_scale, int w_per_channel,
+                       const float *out_scale, void *y, int out_dtype, cudaStream_t stream) {
+    SkinnyArgs args{w, a, M, N, K, a_scale, w_scale, w_per_channel, out_scale, y, out_dtype};
+    return launch<kXE4M3>(args, stream);
+}
+
+}  // namespace fp8l
+
+extern "C" int fp8_w8a16_mm(const void *x, int x_dtype, const uint8_t *w, const float *w_scale,
+                            int64_t M, int64_t N, int64_t K, void *y, void *stream) {
+    using namespace fp8l;
+    if (x_dtype != FP8L_F16 && x_dtype != FP8L_BF16) return FP8L_EINVAL;
+    if (M < 0 || M > 0x7FFFFFFF || N <= 0 || K <= 0 || N > (1 << 20) || K > (1 << 20) ||
+        N % 16 != 0 || K % 16 != 0)
+        return FP8L_ESHAPE;
+    if (w == nullptr || w_scale == nullptr || (M > 0 && (x == nullptr || y == nullptr)))
+        return FP8L_EINVAL;
+    if (!aligned16(w) || (M > 0 && (!aligned16(x) || !aligned16(y))) ||
+        (reinterpret_cast<uintptr_t>(w_scale) & 3u) != 0)
+        return FP8L_EALIGN;
+    int st = check_device(nullptr);
+    if (st != FP8L_OK) return st;
+    SkinnyArgs args{w, x, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                    nullptr, w_scale, 1, nullptr, y, x_dtype};
+    if (x_dtype == FP8L_F16) return launch<kXF16>(args, as_stream(stream));
+    return launch<kXBF16>(args, as_stream(stream));
+}

@@ -1,0 +1,176 @@
+/*
+ * fp8linear.h - C ABI of the FP8 E4M3 quantized linear layer for one NVIDIA
+ * GB300 GPU (sm_103a).
+ *
+ * The layer (page titles and the parts of the pages that define it):
+ *  - "[Kernel][FP8] Initial support with dynamic per-tensor scaling",
+ *    Algorithm: weights are quantized once with a per-tensor scale; the
+ *    activation scale is computed in every forward pass; the forward pass is
+ *    a cast to float8_e4m3fn followed by a scaled matrix product
+ *    (torch._scaled_mm in the microbenchmark list).
+ *  - "RFC: FP8 Quantization Schema in vLLM", Scope and Interface Content:
+ *    OCP FP8_E4M3 numbers; static input scales; an output scale that lets a
+ *    GEMM emit FP8_E4M3 directly (the output_scale discussion).
+ *  - "Marlin fp8", kernel argument checks: a weight-only FP8 product for
+ *    16-bit activations whose weight scale is one value per output channel
+ *    (b_scales of shape [1, N]).
+ *  - "RFC: FP8 Quantization Schema in vLLM", the gate_proj question: FP8 GEMM
+ *    shapes must be divisible by 16.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *    library never allocates, frees or keeps device memory between calls.
+ *  - Tensors are dense and row-major: X / A are [M, K], W is [N, K] (the
+ *    nn.Linear layout; both product operands have K contiguous), Y is [M, N].
+ *  - E4M3 tensors are arrays of uint8 codes (OCP float8_e4m3fn bit patterns).
+ *  - Scales are float32 values in DEVICE memory, so a dynamic scale written
+ *    by one call is consumed by the next without a host round trip.
+ *  - Tensor pointers must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *    only enqueue work: they return before the GPU finishes, never
+ *    synchronize, and a return of FP8L_OK means the work was launched.
+ *  - Errors found on the host (FP8L_EINVAL, FP8L_ESHAPE, FP8L_EALIGN,
+ *    FP8L_EUNSUPPORTED) are returned before anything is launched and leave
+ *    every output untouched.  FP8L_ECUDA reports a failed CUDA call or
+ *    launch.  Device-side wait time-outs are recorded in the workspace and
+ *    reported by fp8l_read_status().
+ *  - Inputs must be finite.  NaN or Inf input is outside the contract.
+ */
+#ifndef FP8LINEAR_H
+#define FP8LINEAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FP8L_ABI_VERSION 1
+
+/* Only the entry points below are exported from the shared library. */
+#if defined(__GNUC__)
+#define FP8L_API __attribute__((visibility("default")))
+#else
+#define FP8L_API
+#endif
+
+/* Status codes returned by every entry point. */
+enum fp8l_status {
+    FP8L_OK = 0,
+    FP8L_EINVAL = 1,      /* null pointer, unknown dtype or flag value      */
+    FP8L_ESHAPE = 2,      /* a size is negative, too large, or breaks a
+                             multiple-of-16 rule                            */
+    FP8L_EALIGN = 3,      /* a tensor pointer is not 16-byte aligned        */
+    FP8L_ECUDA = 4,       /* a CUDA call or kernel launch failed            */
+    FP8L_ETIMEOUT = 5,    /* a device-side wait gave up (fp8l_read_status)  */
+    FP8L_EUNSUPPORTED = 6 /* the current device is not compute capability
+                             10.3, or the dtype combination is unsupported  */
+};
+
+/* Element types. */
+enum fp8l_dtype {
+    FP8L_F16 = 0,   /* IEEE binary16                                         */
+    FP8L_BF16 = 1,  /* bfloat16                                              */
+    FP8L_E4M3 = 2,  /* OCP float8_e4m3fn code (uint8)                        */
+    FP8L_F32 = 3    /* IEEE binary32 (quantizer input only)                  */
+};
+
+/* Size in bytes of the workspace that fp8_quant_per_tensor (dynamic mode)
+ * and fp8_scaled_mm need.  The caller allocates it once (device memory,
+ * 16-byte aligned), fills it with zeros once, and may reuse it for every
+ * later call on streams that do not run those calls concurrently.  It holds
+ * a device status word and the per-block partial maxima of the dynamic
+ * quantizer; the library keeps nothing else in it between calls. */
+FP8L_API size_t fp8l_workspace_bytes(void);
+
+/* Per-tensor quantization of a [rows, cols] activation or weight tensor
+ * to E4M3 ("[Kernel][FP8] Initial support with dynamic per-tensor scaling",
+ * Algorithm; static scales: "RFC: FP8 Quantization Schema in vLLM", Scope).
+ *
+ *   dynamic != 0:  amax  = max_i |x_i|                       (exact)
+ *                  s     = amax / 448  (one fp32 IEEE division; s = 1 when
+ *                          that quotient is 0, i.e. for an all-zero tensor)
+ *                  *scale = s is written to device memory
+ *   dynamic == 0:  s = *scale is read from device memory (a static,
+ *                  calibrated input_scale); it must be positive and finite
+ *   every element: q_i = E4M3(fp32(x_i / s)), the quotient being one fp32
+ *                  IEEE division and E4M3() the saturating
+ *                  round-to-nearest-even cast (|v| >= 448 gives +-448; the
+ *                  sign is kept, so negatives that round to 0 give 0x80).
+ *
+ * x:         [rows, cols] of x_dtype (FP8L_F16, FP8L_BF16 or FP8L_F32).
+ * q:         [rows, cols] uint8 codes (output).
+ * scale:     one float (output when dynamic, input otherwise).
+ * workspace: fp8l_workspace_bytes() bytes; may be NULL when dynamic == 0.
+ * rows*cols may be 0 (then only the dynamic scale, 1.0f, is written) and
+ * at most 2^40.  The result is bit-for-bit deterministic. */
+FP8L_API int fp8_quant_per_tensor(const void *x, int x_dtype, int64_t rows, int64_t cols,
+                         uint8_t *q, float *scale, int dynamic,
+                         void *workspace, void *stream);
+
+/* Per-row quantization, one dynamic scale per row: the per-output-channel
+ * weight scale of "Marlin fp8" (b_scales [1, N]).  Row r is quantized
+ * exactly as fp8_quant_per_tensor(dynamic=1) would quantize it alone, and
+ * its scale is written to row_scale[r].  Used once after weights are loaded
+ * ("[Kernel][FP8] Initial support ...", Algorithm).
+ *
+ * x: [rows, cols] of x_dtype (FP8L_F16, FP8L_BF16 or FP8L_F32);
+ * q: [rows, cols] uint8; row_scale: [rows] float.  cols must be a multiple
+ * of 16 and at most 2^20; rows at most 2^31 - 1. */
+FP8L_API int fp8_quant_per_row(const void *x, int x_dtype, int64_t rows, int64_t cols,
+                      uint8_t *q, float *row_scale, void *stream);
+
+/* W8A8 scaled matrix product ("[Kernel][FP8] Initial support ...",
+ * torch._scaled_mm; per-channel weight scales: "Marlin fp8"; E4M3 output
+ * through output_scale: "RFC: FP8 Quantization Schema in vLLM").
+ *
+ *   acc[m,n] = sum_k dec(a[m,k]) * dec(w[n,k])      (fp32 accumulation)
+ *   v[m,n]   = acc[m,n] * a_scale[0] * ws(n)        ws(n) = w_scale[n] when
+ *                                                   w_per_channel, else w_scale[0]
+ *   out_dtype FP8L_BF16 / FP8L_F16: y[m,n] = v[m,n] rounded to nearest
+ *   out_dtype FP8L_E4M3:            y[m,n] = E4M3(v[m,n] / out_scale[0])
+ *
+ * a: [M, K] E4M3 codes; w: [N, K] E4M3 codes; y: [M, N] of out_dtype.
+ * a_scale: 1 float; w_scale: 1 or N floats; out_scale: 1 float, required
+ * when out_dtype is FP8L_E4M3 and ignored otherwise.
+ * M >= 0 (M == 0 launches nothing); N and K are positive multiples of 16
+ * (the FP8 GEMM shape rule), N, K <= 2^20, M <= 2^31 - 1.
+ * M <= 16 runs a weight-streaming kernel; larger M runs the tcgen05 tensor
+ * core kernel.  workspace: fp8l_workspace_bytes() bytes (status word). */
+FP8L_API int fp8_scaled_mm(const uint8_t *a, const uint8_t *w, int64_t M, int64_t N,
+                  int64_t K, const float *a_scale, const float *w_scale,
+                  int w_per_channel, const float *out_scale, void *y,
+                  int out_dtype, void *workspace, void *stream);
+
+/* W8A16 weight-only product ("Marlin fp8"): 16-bit activations times E4M3
+ * weights with one scale per output channel.
+ *
+ *   y[m,n] = w_scale[n] * sum_k x[m,k] * dec(w[n,k])  (fp32 accumulation,
+ *            rounded to nearest in x_dtype)
+ *
+ * x: [M, K] of x_dtype (FP8L_F16 or FP8L_BF16); w: [N, K] E4M3 codes;
+ * w_scale: [N] floats; y: [M, N] of x_dtype.  M >= 0; N and K positive
+ * multiples of 16, at most 2^20.  Built for decode batches (M <= 16); a
+ * larger M is computed correctly in groups of 16 rows, each group
+ * re-reading W. */
+FP8L_API int fp8_w8a16_mm(const void *x, int x_dtype, const uint8_t *w,
+                 const float *w_scale, int64_t M, int64_t N, int64_t K,
+                 void *y, void *stream);
+
+/* Waits for `stream`, then reads and clears the workspace's status word.
+ * Returns FP8L_OK, FP8L_ETIMEOUT if a device-side wait of an earlier call
+ * gave up (that call's outputs are then undefined), or FP8L_ECUDA. */
+FP8L_API int fp8l_read_status(void *workspace, void *stream);
+
+/* Static, human-readable name of a status code. */
+FP8L_API const char *fp8l_strerror(int status);
+
+/* FP8L_ABI_VERSION of the built library. */
+FP8L_API int fp8l_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8LINEAR_H */

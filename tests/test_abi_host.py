@@ -1,0 +1,142 @@
+"""Host-side checks of the C ABI: the library builds, loads without a GPU,
+exports every entry point the header declares, and rejects bad arguments
+before touching CUDA.  No kernel is launched here."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8linear.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp8_quantized_linear_gb300 import build
+    build.build()
+    import fp8_quantized_linear_gb300 as fl
+    return fl.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(fp8\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("fp8_quant_per_tensor", "fp8_quant_per_row", "fp8_scaled_mm", "fp8_w8a16_mm",
+                 "fp8l_workspace_bytes", "fp8l_read_status", "fp8l_strerror", "fp8l_abi_version"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from fp8_quantized_linear_gb300 import LIB_PATH
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_only_c_abi_symbols_exported(lib):
+    from fp8_quantized_linear_gb300 import LIB_PATH
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert all(n.startswith("fp8") for n in exported), sorted(n for n in exported if not n.startswith("fp8"))
+
+
+def test_constants(lib):
+    import fp8_quantized_linear_gb300 as fl
+    assert lib.fp8l_abi_version() == 1
+    assert fl.fp8l_workspace_bytes() >= 4096 and fl.fp8l_workspace_bytes() % 16 == 0
+    for code in range(7):
+        assert fl.strerror(code)
+    assert "unknown" in fl.strerror(99)
+
+
+P = ctypes.c_void_p
+A16 = 0x10000  # a fake, 16-byte aligned address: never dereferenced
+
+
+def test_scaled_mm_argument_errors(lib):
+    import fp8_quantized_linear_gb300._binding as b
+    f = lib.fp8_scaled_mm
+    ok = dict(a=A16, w=A16, M=32, N=32, K=32, sa=A16, sw=A16, pc=0, os=None, y=A16,
+              od=b.BF16, ws=A16, st=None)
+
+    def call(**kw):
+        d = dict(ok)
+        d.update(kw)
+        return f(d["a"], d["w"], d["M"], d["N"], d["K"], d["sa"], d["sw"], d["pc"], d["os"],
+                 d["y"], d["od"], d["ws"], d["st"])
+    assert call(od=7) == b.EINVAL
+    assert call(sa=None) == b.EINVAL
+    assert call(w=None) == b.EINVAL
+    assert call(ws=None) == b.EINVAL
+    assert call(od=b.E4M3, os=None) == b.EINVAL
+    assert call(N=24) == b.ESHAPE
+    assert call(K=8) == b.ESHAPE
+    assert call(K=0) == b.ESHAPE
+    assert call(M=-1) == b.ESHAPE
+    assert call(N=(1 << 20) + 16) == b.ESHAPE
+    assert call(a=None) == b.EINVAL
+    assert call(a=A16 + 8) == b.EALIGN
+    assert call(y=A16 + 4) == b.EALIGN
+    assert call(sw=A16 + 2) == b.EALIGN
+
+
+def test_w8a16_argument_errors(lib):
+    import fp8_quantized_linear_gb300._binding as b
+    f = lib.fp8_w8a16_mm
+    assert f(A16, b.E4M3, A16, A16, 1, 32, 32, A16, None) == b.EINVAL
+    assert f(A16, b.F32, A16, A16, 1, 32, 32, A16, None) == b.EINVAL
+    assert f(A16, b.F16, A16, A16, 1, 40, 32, A16, None) == b.ESHAPE
+    assert f(A16, b.F16, A16, A16, 1, 32, 40, A16, None) == b.ESHAPE
+    assert f(A16, b.F16, None, A16, 1, 32, 32, A16, None) == b.EINVAL
+    assert f(A16 + 2, b.F16, A16, A16, 1, 32, 32, A16, None) == b.EALIGN
+
+
+def test_quant_argument_errors(lib):
+    import fp8_quantized_linear_gb300._binding as b
+    f = lib.fp8_quant_per_tensor
+    assert f(A16, b.E4M3, 4, 4, A16, A16, 1, A16, None) == b.EINVAL
+    assert f(A16, b.BF16, 4, 4, A16, None, 1, A16, None) == b.EINVAL
+    assert f(A16, b.BF16, 4, 4, A16, A16, 1, None, None) == b.EINVAL
+    assert f(A16, b.BF16, -1, 4, A16, A16, 1, A16, None) == b.ESHAPE
+    assert f(A16, b.BF16, 1 << 30, 1 << 20, A16, A16, 1, A16, None) == b.ESHAPE
+    assert f(A16 + 8, b.BF16, 4, 4, A16, A16, 1, A16, None) == b.EALIGN
+    assert f(A16, b.BF16, 4, 4, A16, A16 + 1, 1, A16, None) == b.EALIGN
+    g = lib.fp8_quant_per_row
+    assert g(A16, b.BF16, 4, 24, A16, A16, None) == b.ESHAPE
+    assert g(A16, 9, 4, 32, A16, A16, None) == b.EINVAL
+    assert g(A16, b.BF16, 4, 32, None, A16, None) == b.EINVAL
+
+
+def test_read_status_argument_errors(lib):
+    import fp8_quantized_linear_gb300._binding as b
+    assert lib.fp8l_read_status(None, None) == b.EINVAL
+    assert lib.fp8l_read_status(A16 + 4, None) == b.EALIGN
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    import fp8_quantized_linear_gb300._binding as b
+    monkeypatch.setattr(b, "_lib", None)
+    monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "nope.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        b.load()
+
+
+def test_product_path_does_not_touch_the_oracle():
+    pkg = os.path.join(ROOT, "fp8_quantized_linear_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert not re.search(r"\boracle\b", text), os.path.join(dirpath, fn)
+                assert "fp8_oracle" not in text

@@ -1,0 +1,144 @@
+"""GPU parity of the per-tensor / per-row E4M3 quantizer: codes and scales
+must equal the oracle's bit for bit ("[Kernel][FP8] Initial support with
+dynamic per-tensor scaling", Algorithm; "RFC: FP8 Quantization Schema in
+vLLM", static input scale)."""
+import numpy as np
+import pytest
+import torch
+
+import fp8_quantized_linear_gb300 as fl
+import oracle
+import pins
+import synthetic
+from gpu_util import DEV, assert_status_ok, dev, host, scalar
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = [torch.bfloat16, torch.float16, torch.float32]
+
+
+def _check_dynamic(x):
+    q, s = fl.fp8_quant_per_tensor(dev(x))
+    q_o, s_o = oracle.quant_per_tensor(x)
+    qh = host(q)
+    assert np.float32(host(s)[0]) == s_o, (host(s)[0], s_o)
+    bad = np.nonzero(qh.reshape(-1) != q_o.reshape(-1))[0]
+    assert bad.size == 0, (x.dtype, tuple(x.shape), bad[:8], qh.reshape(-1)[bad[:8]], q_o.reshape(-1)[bad[:8]])
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", [(1, 1), (1, 15), (1, 16), (1, 17), (3, 33), (16, 512),
+                                   (37, 1000), (129, 4112), (1024, 4096)])
+def test_dynamic_matches_oracle(dtype, shape):
+    x = synthetic.activation(shape[0], shape[1], dtype, seed=shape[0] * 131 + shape[1])
+    _check_dynamic(x)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_dynamic_outlier_channels(dtype):
+    # prefill workload: 1% of K channels scaled by 50 (many small codes,
+    # E4M3 subnormals)
+    x = synthetic.activation(1024, 4096, dtype, seed=3000, outlier_frac=0.01)
+    _check_dynamic(x)
+
+
+def test_dynamic_llama_sizes():
+    for (M, K) in ((8192, 4096), (8192, 14336)):
+        _check_dynamic(synthetic.activation(M, K, torch.bfloat16, seed=M + K))
+
+
+def test_empty_and_zero():
+    x = torch.zeros((0, 64), dtype=torch.bfloat16)
+    q, s = fl.fp8_quant_per_tensor(dev(x))
+    assert host(s)[0] == 1.0 and q.numel() == 0
+    x = torch.zeros((5, 48), dtype=torch.float16)
+    q, s = fl.fp8_quant_per_tensor(dev(x))
+    assert host(s)[0] == 1.0 and not host(q).any()
+    x = -torch.zeros((2, 16), dtype=torch.float32)  # negative zeros keep their sign
+    _check_dynamic(x)
+
+
+def test_worked_examples():
+    def quant(x, scale=None):
+        q, s = fl.fp8_quant_per_tensor(dev(x.reshape(1, -1)))
+        return host(q).reshape(-1), np.float32(host(s)[0])
+    pins.check_quant_worked(quant)
+
+
+def test_single_huge_element_and_ties():
+    # amax set by one element; every other element sits on an E4M3 tie after
+    # division by s = 2^-6
+    table = oracle.decode_table()
+    pos = table[:127]
+    mids = ((pos[:-1] + pos[1:]) / 2) / 64.0
+    vals = np.concatenate([[7.0], mids, -mids]).astype(np.float32)
+    _check_dynamic(torch.from_numpy(vals).reshape(1, -1))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("scale", [1.0, 0.0123, 3.0517578125e-05, 7.0])
+def test_static_every_16bit_value(dtype, scale):
+    # every finite value of the format, static scale: exhaustive cast check
+    v = torch.from_numpy(pins.all_16bit_values(dtype)).to(dtype)
+    x = v.reshape(1, -1)
+    q, _ = fl.fp8_quant_per_tensor(dev(x), scale=scalar(scale), dynamic=False)
+    q_o, _ = oracle.quant_per_tensor(x, scale=np.float32(scale))
+    assert np.array_equal(host(q).reshape(-1), q_o.reshape(-1))
+
+
+def test_static_float32_midpoint_neighbourhoods():
+    # every E4M3 rounding midpoint and 64 float32 neighbours on each side
+    table = oracle.decode_table()
+    pos = table[:127]
+    mids = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)
+    mids = np.concatenate([mids, np.float32([448.0, 464.0, 480.0, 1e6])])
+    bits = mids.view(np.int32)
+    offs = np.arange(-64, 65, dtype=np.int32)
+    v = (bits[:, None] + offs[None, :]).reshape(-1).view(np.float32)
+    v = np.concatenate([v, -v])
+    x = torch.from_numpy(v).reshape(1, -1)
+    for scale in (1.0, 0.5, 0.1, 1e-3):
+        q, _ = fl.fp8_quant_per_tensor(dev(x), scale=scalar(scale), dynamic=False)
+        q_o, _ = oracle.quant_per_tensor(x, scale=np.float32(scale))
+        assert np.array_equal(host(q).reshape(-1), q_o.reshape(-1)), scale
+
+
+def test_static_random_float32():
+    g = torch.Generator().manual_seed(77)
+    x = (torch.randn(1 << 20, generator=g) * torch.exp2(torch.randint(-30, 20, (1 << 20,), generator=g).float()))
+    for scale in (1.0, 0.37, 2.5e-4):
+        q, _ = fl.fp8_quant_per_tensor(dev(x.reshape(64, -1)), scale=scalar(scale), dynamic=False)
+        q_o, _ = oracle.quant_per_tensor(x, scale=np.float32(scale))
+        assert np.array_equal(host(q).reshape(-1), q_o.reshape(-1)), scale
+
+
+def test_repeat_and_workspace_reuse():
+    # stale partials from a larger earlier call must not leak into a smaller one
+    big = synthetic.activation(4096, 4096, torch.bfloat16, seed=5) * 10
+    small = synthetic.activation(4, 64, torch.bfloat16, seed=6)
+    fl.fp8_quant_per_tensor(dev(big))
+    _check_dynamic(small)
+    q1, s1 = fl.fp8_quant_per_tensor(dev(small))
+    q2, s2 = fl.fp8_quant_per_tensor(dev(small))
+    assert torch.equal(q1, q2) and torch.equal(s1, s2)
+    assert_status_ok()
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", [(1, 16), (7, 48), (256, 512), (300, 4096)])
+def test_per_row_matches_oracle(dtype, shape):
+    w = synthetic.weight(shape[0], shape[1], dtype, seed=shape[0] + 7 * shape[1])
+    if shape[0] > 3:
+        w[3] = 0  # an all-zero row gets scale 1
+    q, s = fl.fp8_quant_per_row(dev(w))
+    q_o, s_o = oracle.quant_per_row(w)
+    assert np.array_equal(host(s), s_o)
+    assert np.array_equal(host(q), q_o)
+
+
+def test_per_row_large():
+    w = synthetic.weight(8192, 8192, torch.bfloat16, seed=11)
+    q, s = fl.fp8_quant_per_row(dev(w))
+    q_o, s_o = oracle.quant_per_row(w)
+    assert np.array_equal(host(s), s_o)
+    assert np.array_equal(host(q), q_o)

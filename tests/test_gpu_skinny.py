@@ -1,0 +1,118 @@
+"""GPU parity of the weight-streaming kernels: W8A16 ("Marlin fp8": 16-bit
+activations, E4M3 weights, one scale per output channel) and the small-M
+branch of the W8A8 scaled product."""
+import numpy as np
+import pytest
+import torch
+
+import fp8_quantized_linear_gb300 as fl
+import oracle
+import synthetic
+from gpu_util import assert_e4m3_close, assert_gemm_close, dev, host, scalar
+
+pytestmark = pytest.mark.gpu
+
+
+def _w8a16_case(M, N, K, xdtype, seed):
+    x = synthetic.activation(M, K, xdtype, seed=seed)
+    w = synthetic.weight(N, K, torch.bfloat16, seed=seed)
+    qw, sw = oracle.quant_per_row(w)
+    y = fl.fp8_w8a16_mm(dev(x), dev(qw), dev(sw))
+    assert y.dtype == xdtype
+    return host(y), oracle.w8a16_ref(x, qw, sw)
+
+
+@pytest.mark.parametrize("xdtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("M,N,K", [(1, 16, 16), (1, 32, 80), (3, 48, 208), (8, 256, 512),
+                                   (9, 64, 1024), (16, 272, 4096), (17, 64, 256), (40, 80, 144)])
+def test_w8a16_small(M, N, K, xdtype):
+    y, y_ref = _w8a16_case(M, N, K, xdtype, seed=M * 1000 + N + K)
+    assert_gemm_close(y, y_ref, (M, N, K, xdtype))
+
+
+@pytest.mark.parametrize("shape_idx", range(12))
+def test_w8a16_decode_workload(shape_idx):
+    wl = synthetic.WORKLOADS["decode_w8a16"]
+    M, N, K = wl.shapes[shape_idx]
+    y, y_ref = _w8a16_case(M, N, K, torch.float16, seed=wl.seed(shape_idx))
+    assert_gemm_close(y, y_ref, (M, N, K))
+
+
+def test_w8a16_exact_integer_and_distinct_channel_scales():
+    # all-ones weights, integer activations, power-of-two per-channel scales:
+    # fp32 accumulation is exact, so each output equals the closed form
+    # sw[n] * sum_k x[m,k] exactly (a scale applied to the wrong column, the
+    # bug of a kernel that only worked with a repeated scalar scale, fails)
+    M, N, K = 5, 64, 512
+    g = torch.Generator().manual_seed(4)
+    x = torch.randint(-3, 4, (M, K), generator=g).to(torch.float16)
+    qw = np.full((N, K), 0x38, np.uint8)
+    sw = np.array([2.0 ** (n % 7 - 3) for n in range(N)], np.float32)
+    y = host(fl.fp8_w8a16_mm(dev(x), dev(qw), dev(sw)))
+    want = x.double().sum(1, keepdim=True).numpy() * sw[None, :].astype(np.float64)
+    assert np.array_equal(y, want)
+
+
+def test_w8a16_permutation_weights():
+    # W is a permutation matrix: y[m, n] = sw[n] * x[m, pi(n)] exactly
+    K = N = 256
+    pi = (np.arange(N) * 37 + 11) % K
+    qw = np.zeros((N, K), np.uint8)
+    qw[np.arange(N), pi] = 0x38
+    sw = np.array([2.0 ** (n % 5 - 2) for n in range(N)], np.float32)
+    x = synthetic.activation(7, K, torch.float16, seed=9)
+    y = host(fl.fp8_w8a16_mm(dev(x), dev(qw), dev(sw)))
+    want = x.double().numpy()[:, pi] * sw[None, :]
+    assert np.array_equal(y, want.astype(np.float16).astype(np.float32))
+
+
+def test_w8a16_empty_batch():
+    x = torch.zeros((0, 64), dtype=torch.float16)
+    qw = np.zeros((32, 64), np.uint8)
+    y = fl.fp8_w8a16_mm(dev(x), dev(qw), dev(np.ones(32, np.float32)))
+    assert y.shape == (0, 32)
+
+
+def _w8a8_small(M, N, K, per_channel, out, seed):
+    x = synthetic.activation(M, K, torch.bfloat16, seed=seed)
+    w = synthetic.weight(N, K, torch.bfloat16, seed=seed)
+    qa, sa = oracle.quant_per_tensor(x)
+    if per_channel:
+        qw, sw = oracle.quant_per_row(w)
+    else:
+        qw, s = oracle.quant_per_tensor(w)
+        sw = np.array([s], np.float32)
+    y_ref = oracle.scaled_mm_ref(qa, qw, sa, sw)
+    if out == "e4m3":
+        os_ = np.float32(np.abs(y_ref).max() / 448.0 * 0.75)  # a few outputs saturate
+        y = fl.fp8_scaled_mm(dev(qa), dev(qw), scalar(sa), dev(sw), out_dtype=torch.uint8,
+                             out_scale=scalar(os_))
+        assert_e4m3_close(host(y), y_ref, os_, (M, N, K))
+    else:
+        dt = torch.bfloat16 if out == "bf16" else torch.float16
+        y = fl.fp8_scaled_mm(dev(qa), dev(qw), scalar(sa), dev(sw), out_dtype=dt)
+        assert_gemm_close(host(y), y_ref, (M, N, K, out))
+
+
+@pytest.mark.parametrize("out", ["bf16", "fp16", "e4m3"])
+@pytest.mark.parametrize("per_channel", [False, True])
+@pytest.mark.parametrize("M,N,K", [(1, 16, 16), (1, 256, 512), (5, 48, 80), (16, 256, 512),
+                                   (16, 4096, 4096), (1, 28672, 4096), (16, 4096, 14336)])
+def test_w8a8_small_m(M, N, K, per_channel, out):
+    _w8a8_small(M, N, K, per_channel, out, seed=M + N + K)
+
+
+def test_w8a8_small_m_exact_integer():
+    # codes in {-2,-1,-0.5,0,0.5,1,2}: fp32 accumulation is exact; with
+    # power-of-two scales the bf16 output equals the rounded exact value
+    vals = {0x40: 2.0, 0x38: 1.0, 0x30: 0.5, 0x00: 0.0, 0xB0: -0.5, 0xB8: -1.0, 0xC0: -2.0}
+    codes = np.array(list(vals), np.uint8)
+    rng = np.random.default_rng(12)
+    M, N, K = 16, 128, 1024
+    qa = codes[rng.integers(0, 7, (M, K))]
+    qw = codes[rng.integers(0, 7, (N, K))]
+    sw = np.array([2.0 ** -(n % 4) for n in range(N)], np.float32)
+    y = host(fl.fp8_scaled_mm(dev(qa), dev(qw), scalar(0.5), dev(sw), out_dtype=torch.bfloat16))
+    exact = oracle.scaled_mm_bruteforce(qa, qw, np.float32(0.5), sw)
+    want = torch.from_numpy(exact).to(torch.bfloat16).float().numpy()
+    assert np.array_equal(y, want)
