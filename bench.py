@@ -106,6 +106,14 @@ def reduce_max(value: float, world: int, device) -> float:
     return float(t.item())
 
 
+def aggregate(units_per_step: float, ms_per_step: float, world: int, unit: str) -> float:
+    """Whole-job throughput of N replicas: every rank processes the same
+    units per step; the step time is the maximum over ranks."""
+    sec = ms_per_step / 1e3
+    scale = 1e9 if unit == "GB/s" else 1e12
+    return units_per_step * world / sec / scale
+
+
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -558,10 +566,8 @@ def run_ours(args):
     sampler.stop()
     clocks = sampler.summary(res["window"][1], res["window"][2], res["window"][0])
     b, f = work.step_units()
-    sec = res["ms_per_step"] / 1e3
     unit = work.headline_unit()
-    per_rank = (b / sec / 1e9) if unit == "GB/s" else (f / sec / 1e12)
-    value = per_rank * world
+    value = aggregate(b if unit == "GB/s" else f, res["ms_per_step"], world, unit)
     rf, kinds = roofline(res["per_kind"], peaks)
     # end to end through the public API with host buffers
     e2e_steps = max(3, min(args.steps, 50))
