@@ -327,3 +327,94 @@ extern "C" int fp8_quant_per_row(const void *x, int x_dtype, int64_t rows, int64
         default: return run_per_row<FP8L_F32>(x, rows, cols, q, row_scale, s);
     }
 }
+
+// ---------------------------------------------------------------------------
+// Dynamic per-tensor quantization without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory: a plug-in that runs inside a
+// host framework which owns every device allocation through its own pool and
+// forbids direct cudaMalloc, or a serving loop that fixed its memory
+// footprint at start-up and has no way to hand a workspace down to this
+// call.  For them, the per-block partial maxima live in the array below,
+// which is part of the library image: every GPU that loads the library holds
+// it (8 KiB) until the process exits.
+#include <atomic>
+
+namespace fp8l {
+namespace {
+
+constexpr int kNoallocMaxPartials = 2048;  // partial maxima the array holds
+static __device__ __align__(256) float g_noalloc_partials[kNoallocMaxPartials];
+
+constexpr int kNoallocMaxDevices = 64;
+std::atomic<float *> g_noalloc_ptr[kNoallocMaxDevices];
+
+// Device address of g_noalloc_partials on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address comes from
+// cudaGetSymbolAddress, once per device, with that device current.
+int noalloc_scratch(float **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FP8L_ECUDA;
+    if (dev < 0 || dev >= kNoallocMaxDevices) return FP8L_EUNSUPPORTED;
+    float *p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_noalloc_partials) != cudaSuccess || addr == nullptr)
+            return FP8L_ECUDA;
+        p = static_cast<float *>(addr);
+        g_noalloc_ptr[dev].store(p, std::memory_order_release);
+    }
+    *out = p;
+    return FP8L_OK;
+}
+
+template <int DT>
+int run_noalloc(const void *x, int64_t numel, uint8_t *q, float *scale, float *part,
+                cudaStream_t stream, int sms) {
+    const int64_t n_chunks = numel / kChunk;
+    int n_part = 0;
+    if (numel > 0) {
+        // every block writes its own partial and the cast kernel reads exactly
+        // the n_part entries this call wrote, so nothing needs clearing
+        int64_t blocks = (n_chunks + 2 * kThreads - 1) / (2 * kThreads);
+        if (blocks < 1) blocks = 1;
+        if (blocks > int64_t(sms) * 8) blocks = int64_t(sms) * 8;
+        if (blocks > kNoallocMaxPartials) blocks = kNoallocMaxPartials;
+        n_part = static_cast<int>(blocks);
+        absmax_kernel<DT><<<n_part, kThreads, 0, stream>>>(x, numel, part);
+        if (launch_status() != FP8L_OK) return FP8L_ECUDA;
+    }
+    const int64_t need = (n_chunks + kThreads - 1) / kThreads;
+    const int64_t cap = int64_t(sms) * 8;
+    const int cast_blocks = static_cast<int>(need < 1 ? 1 : (need < cap ? need : cap));
+    cast_kernel<DT, true><<<cast_blocks, kThreads, 0, stream>>>(x, numel, q, scale, part, n_part);
+    return launch_status();
+}
+
+}  // namespace
+}  // namespace fp8l
+
+extern "C" int fp8_quant_per_tensor_noalloc(const void *x, int x_dtype, int64_t rows,
+                                            int64_t cols, uint8_t *q, float *scale,
+                                            void *stream) {
+    using namespace fp8l;
+    if (!valid_in_dtype(x_dtype) || scale == nullptr) return FP8L_EINVAL;
+    if (rows < 0 || cols < 0) return FP8L_ESHAPE;
+    if (cols != 0 && rows > kMaxNumel / cols) return FP8L_ESHAPE;
+    const int64_t numel = rows * cols;
+    if (numel > 0 && (x == nullptr || q == nullptr)) return FP8L_EINVAL;
+    if (numel > 0 && (!aligned16(x) || !aligned16(q))) return FP8L_EALIGN;
+    if ((reinterpret_cast<uintptr_t>(scale) & 3u) != 0) return FP8L_EALIGN;
+    int sms = 0;
+    int st = check_device(&sms);
+    if (st != FP8L_OK) return st;
+    float *part = nullptr;
+    st = noalloc_scratch(&part);
+    if (st != FP8L_OK) return st;
+    cudaStream_t s = as_stream(stream);
+    switch (x_dtype) {
+        case FP8L_F16: return run_noalloc<FP8L_F16>(x, numel, q, scale, part, s, sms);
+        case FP8L_BF16: return run_noalloc<FP8L_BF16>(x, numel, q, scale, part, s, sms);
+        default: return run_noalloc<FP8L_F32>(x, numel, q, scale, part, s, sms);
+    }
+}

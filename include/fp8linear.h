@@ -158,6 +158,35 @@ FP8L_API int fp8_w8a16_mm(const void *x, int x_dtype, const uint8_t *w,
                  const float *w_scale, int64_t M, int64_t N, int64_t K,
                  void *y, void *stream);
 
+/* Dynamic per-tensor quantization that allocates nothing and takes no
+ * workspace.  The pages have no counterpart to this entry point.
+ *
+ * It is for callers that cannot allocate device memory themselves: for
+ * example a plug-in running inside a framework that owns every device
+ * allocation through its own pool, or a serving loop whose memory footprint
+ * is fixed at start-up and that has no workspace to pass down.  It computes
+ * exactly what fp8_quant_per_tensor computes with dynamic != 0 (same codes,
+ * same scale, bit for bit), with the same arguments minus `dynamic` and
+ * `workspace`.
+ *
+ * Scratch: the per-block partial maxima live in an 8 KiB array inside the
+ * library image (2048 floats), which every GPU that loads the library holds
+ * until the process exits.  A call never needs more than those 2048 entries,
+ * so every size fp8_quant_per_tensor accepts is accepted here; rows*cols
+ * above 2^40 is rejected with FP8L_ESHAPE.  Every call on a device shares
+ * that one array: calls whose kernels may overlap on the GPU (different
+ * streams without ordering between them) race on it and must not be issued.
+ * Nothing in the array needs to start at zero; each call writes the entries
+ * it reads.
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ * first call before any stream capture begins.  The entry point calls no
+ * cudaMalloc, cudaFree or other allocating routine. */
+FP8L_API int fp8_quant_per_tensor_noalloc(const void *x, int x_dtype, int64_t rows,
+                                          int64_t cols, uint8_t *q, float *scale,
+                                          void *stream);
+
 /* Waits for `stream`, then reads and clears the workspace's status word.
  * Returns FP8L_OK, FP8L_ETIMEOUT if a device-side wait of an earlier call
  * gave up (that call's outputs are then undefined), or FP8L_ECUDA. */
