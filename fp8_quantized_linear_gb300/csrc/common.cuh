@@ -12,6 +12,7 @@ namespace fp8l {
 // ---------------------------------------------------------------------------
 // Workspace layout (fp8l_workspace_bytes bytes, zero-filled by the caller once)
 //   [0, 4)                   uint32 status word (bit flags below)
+//   [4, 8)                   uint32 quantizer ticket counter (zero between calls)
 //   [256, 256 + 4*kMaxParts) float per-block partial maxima of the quantizer
 constexpr size_t kStatusOffset = 0;
 constexpr size_t kPartialsOffset = 256;
@@ -34,6 +35,10 @@ inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s
 
 inline unsigned *status_word(void *workspace) {
     return reinterpret_cast<unsigned *>(static_cast<char *>(workspace) + kStatusOffset);
+}
+
+inline unsigned *ticket_word(void *workspace) {
+    return reinterpret_cast<unsigned *>(static_cast<char *>(workspace) + 4);
 }
 
 inline float *partials(void *workspace) {

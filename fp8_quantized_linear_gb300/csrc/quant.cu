@@ -4,15 +4,21 @@
 // scaling", Algorithm): two bandwidth-bound launches.
 //   1. absmax_kernel: every thread streams 16-element chunks with 16-byte
 //      loads and keeps the running maximum of the magnitude BITS (sign bit
-//      cleared; for finite IEEE values, a larger magnitude has larger unsigned
+//      cleared; for finite IEEE values a larger magnitude has larger unsigned
 //      bits, so the maximum is exact and needs no float compare).  Warp
 //      reduction with redux.sync, block reduction in shared memory, one
-//      partial per block into the workspace.
-//   2. cast_kernel: every block reduces the partials (a few hundred floats,
-//      L2 resident), forms s = amax / 448 (IEEE division, 1 when zero), and
-//      casts its chunks: q = E4M3_satRNE(x / s) with an IEEE division per
-//      element and the hardware saturating RNE conversion.  Block 0 writes s.
-//   The second pass re-reads X; X up to ~100 MB is still in the 126 MB L2.
+//      partial per block.  The last block to finish (a ticket counter; no
+//      block waits for another) reduces the partials, forms s = amax / 448
+//      (one IEEE division; 1 when zero), writes s and resets the counter.
+//   2. cast_kernel: q = E4M3_satRNE(fp32(x / s)) with the hardware saturating
+//      round-to-nearest-even conversion.  The quotient is taken as
+//      x * RN(1/s), which lies within 2 ulps of RN(x / s); where that product
+//      is within 3 ulps of an E4M3 rounding midpoint (every normal-range
+//      midpoint has the low 20 fp32 mantissa bits equal to 0x80000) or below
+//      2^-6 (the E4M3 subnormal range), the IEEE division is taken instead.
+//      Elsewhere both values round to the same code, so the codes equal
+//      those of the division everywhere.
+//   The cast re-reads X, which up to ~100 MB is still in the 126 MB L2.
 // Static mode ("RFC: FP8 Quantization Schema in vLLM", input scales) runs
 // only the cast kernel with s read from device memory.
 #include <cuda_bf16.h>
@@ -119,11 +125,31 @@ __device__ __forceinline__ uint8_t e4m3(float a) {
     return static_cast<uint8_t>(__nv_cvt_float_to_fp8(a, __NV_SATFINITE, __NV_E4M3));
 }
 
-__device__ __forceinline__ uint4 quant_chunk(const float (&f)[kChunk], float s) {
+// A float whose saturating RNE E4M3 code is the code of RN(x / s), given
+// r = RN(1 / s); `fast` is false when r is not a normal float.
+__device__ __forceinline__ float quotient(float x, float s, float r, bool fast) {
+    const float q = x * r;
+    const uint32_t b = __float_as_uint(q) & 0x7FFFFFFFu;
+    const bool tiny = (b - 1u) < 0x3C7FFFFFu;               // 0 < |q| < 2^-6
+    const bool near_mid = ((b & 0xFFFFFu) - 0x7FFFDu) < 7u;  // within 3 ulps of ...8p
+    if (!fast || tiny || near_mid) return __fdiv_rn(x, s);
+    return q;
+}
+
+struct Divisor {
+    float s, r;
+    bool fast;
+    __device__ __forceinline__ explicit Divisor(float scale) : s(scale) {
+        r = __frcp_rn(scale);
+        fast = r >= 1.17549435e-38f && r <= 3.40282347e+38f;
+    }
+    __device__ __forceinline__ float operator()(float x) const { return quotient(x, s, r, fast); }
+};
+
+__device__ __forceinline__ uint4 quant_chunk(const float (&f)[kChunk], const Divisor &d) {
     uint32_t p[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-        p[i] = e4m3x2(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
+    for (int i = 0; i < 8; ++i) p[i] = e4m3x2(d(f[2 * i]), d(f[2 * i + 1]));
     return make_uint4(p[0] | (p[1] << 16), p[2] | (p[3] << 16), p[4] | (p[5] << 16),
                       p[6] | (p[7] << 16));
 }
@@ -150,8 +176,10 @@ __device__ __forceinline__ float scale_from_amax(float amax) {
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads)
-absmax_kernel(const void *__restrict__ x, int64_t numel, float *__restrict__ part) {
+absmax_kernel(const void *__restrict__ x, int64_t numel, float *__restrict__ part,
+              unsigned *__restrict__ ticket, float *__restrict__ scale) {
     __shared__ uint32_t red[33];
+    __shared__ bool last;
     const uint4 *xv = static_cast<const uint4 *>(x);
     const int64_t n_chunks = numel / kChunk;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
@@ -174,40 +202,57 @@ absmax_kernel(const void *__restrict__ x, int64_t numel, float *__restrict__ par
     if (blockIdx.x == 0 && threadIdx.x < tail)
         m = max(m, scalar_mag_bits<DT>(x, n_chunks * kChunk + threadIdx.x));
     m = block_max_u32(m, red);
-    if (threadIdx.x == 0) part[blockIdx.x] = mag_bits_to_float<DT>(m);
+    if (threadIdx.x == 0) {
+        part[blockIdx.x] = mag_bits_to_float<DT>(m);
+        __threadfence();  // the partial is visible before the ticket is taken
+        last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!last) return;
+    // last block: every other block's partial is visible (their fences
+    // precede their tickets); read them past L1
+    __threadfence();
+    uint32_t mm = 0;  // partials are non-negative floats: compare their bits
+    for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += kThreads)
+        mm = max(mm, __float_as_uint(__ldcg(part + i)));
+    mm = block_max_u32(mm, red);
+    if (threadIdx.x == 0) {
+        *scale = scale_from_amax(__uint_as_float(mm));
+        *ticket = 0u;  // ready for the next call
+    }
 }
 
-template <int DT, bool kDynamic>
+template <int DT>
 __global__ void __launch_bounds__(kThreads)
 cast_kernel(const void *__restrict__ x, int64_t numel, uint8_t *__restrict__ q,
-            float *__restrict__ scale, const float *__restrict__ part, int n_part) {
-    __shared__ uint32_t red[33];
-    float s;
-    if constexpr (kDynamic) {
-        uint32_t m = 0;  // partials are non-negative floats: compare their bits
-        for (int i = threadIdx.x; i < n_part; i += kThreads) m = max(m, __float_as_uint(part[i]));
-        m = block_max_u32(m, red);
-        s = scale_from_amax(__uint_as_float(m));
-        if (blockIdx.x == 0 && threadIdx.x == 0) *scale = s;
-    } else {
-        s = __ldg(scale);
-    }
+            const float *__restrict__ scale) {
+    const Divisor d(*scale);
     const uint4 *xv = static_cast<const uint4 *>(x);
     uint4 *qv = reinterpret_cast<uint4 *>(q);
     const int64_t n_chunks = numel / kChunk;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    for (int64_t c = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; c < n_chunks;
-         c += stride) {
+    int64_t c = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    for (; c + stride < n_chunks; c += 2 * stride) {
+        uint4 v0[Elt<DT>::kBytes], v1[Elt<DT>::kBytes];
+        float f[kChunk];
+        load_chunk<DT>(xv, c, v0);
+        load_chunk<DT>(xv, c + stride, v1);
+        chunk_values<DT>(v0, f);
+        qv[c] = quant_chunk(f, d);
+        chunk_values<DT>(v1, f);
+        qv[c + stride] = quant_chunk(f, d);
+    }
+    if (c < n_chunks) {
         uint4 v[Elt<DT>::kBytes];
         float f[kChunk];
         load_chunk<DT>(xv, c, v);
         chunk_values<DT>(v, f);
-        qv[c] = quant_chunk(f, s);
+        qv[c] = quant_chunk(f, d);
     }
     const int64_t tail = numel - n_chunks * kChunk;
     if (blockIdx.x == 0 && threadIdx.x < tail) {
         const int64_t i = n_chunks * kChunk + threadIdx.x;
-        q[i] = e4m3(__fdiv_rn(scalar_value<DT>(x, i), s));
+        q[i] = e4m3(d(scalar_value<DT>(x, i)));
     }
 }
 
@@ -231,43 +276,56 @@ row_quant_kernel(const void *__restrict__ x, int64_t cols, uint8_t *__restrict__
     m = block_max_u32(fold_mag<DT>(m), red);
     const float s = scale_from_amax(mag_bits_to_float<DT>(m));
     if (threadIdx.x == 0) row_scale[r] = s;
+    const Divisor d(s);
     for (int64_t c = threadIdx.x; c < n_chunks; c += kThreads) {
         uint4 v[Elt<DT>::kBytes];
         float f[kChunk];
         load_chunk<DT>(xv, c, v);
         chunk_values<DT>(v, f);
-        qv[c] = quant_chunk(f, s);
+        qv[c] = quant_chunk(f, d);
     }
 }
 
 constexpr int64_t kMaxNumel = int64_t(1) << 40;
 
+// absmax blocks: about two 16-element chunks per thread, at most 8 per SM
+// and at most `max_part` (the room for partial maxima)
+int absmax_blocks(int64_t numel, int sms, int max_part) {
+    const int64_t n_chunks = numel / kChunk;
+    int64_t blocks = (n_chunks + 2 * kThreads - 1) / (2 * kThreads);
+    if (blocks < 1) blocks = 1;
+    if (blocks > int64_t(sms) * 8) blocks = int64_t(sms) * 8;
+    if (blocks > max_part) blocks = max_part;
+    return static_cast<int>(blocks);
+}
+
+int cast_blocks(int64_t numel, int sms) {
+    const int64_t need = (numel / kChunk + 2 * kThreads - 1) / (2 * kThreads);
+    const int64_t cap = int64_t(sms) * 8;
+    return static_cast<int>(need < 1 ? 1 : (need < cap ? need : cap));
+}
+
+// dynamic: absmax (+ scale) then cast; static: cast with the given scale.
+// `part` holds max_part floats; `ticket` is zero between calls.
+template <int DT>
+int run_quant(const void *x, int64_t numel, uint8_t *q, float *scale, bool dynamic, float *part,
+              unsigned *ticket, int max_part, cudaStream_t stream, int sms) {
+    if (dynamic) {
+        absmax_kernel<DT><<<absmax_blocks(numel, sms, max_part), kThreads, 0, stream>>>(
+            x, numel, part, ticket, scale);
+        if (launch_status() != FP8L_OK) return FP8L_ECUDA;
+    }
+    if (numel == 0) return FP8L_OK;
+    cast_kernel<DT><<<cast_blocks(numel, sms), kThreads, 0, stream>>>(x, numel, q, scale);
+    return launch_status();
+}
+
 template <int DT>
 int run_per_tensor(const void *x, int64_t numel, uint8_t *q, float *scale, bool dynamic,
                    void *workspace, cudaStream_t stream, int sms) {
-    const int64_t n_chunks = numel / kChunk;
-    const int64_t cast_blocks_needed = (n_chunks + kThreads - 1) / kThreads;
-    const int cast_blocks = static_cast<int>(
-        cast_blocks_needed < 1 ? 1 : (cast_blocks_needed < int64_t(sms) * 8 ? cast_blocks_needed
-                                                                               : int64_t(sms) * 8));
-    if (!dynamic) {
-        if (numel == 0) return FP8L_OK;
-        cast_kernel<DT, false><<<cast_blocks, kThreads, 0, stream>>>(x, numel, q, scale, nullptr, 0);
-        return launch_status();
-    }
-    float *part = partials(workspace);
-    int n_part = 0;
-    if (numel > 0) {
-        const int64_t want = (n_chunks + 2 * kThreads - 1) / (2 * kThreads);
-        int64_t blocks = want < 1 ? 1 : want;
-        if (blocks > int64_t(sms) * 8) blocks = int64_t(sms) * 8;
-        if (blocks > kMaxPartials) blocks = kMaxPartials;
-        n_part = static_cast<int>(blocks);
-        absmax_kernel<DT><<<n_part, kThreads, 0, stream>>>(x, numel, part);
-        if (launch_status() != FP8L_OK) return FP8L_ECUDA;
-    }
-    cast_kernel<DT, true><<<cast_blocks, kThreads, 0, stream>>>(x, numel, q, scale, part, n_part);
-    return launch_status();
+    float *part = dynamic ? partials(workspace) : nullptr;
+    unsigned *tk = dynamic ? ticket_word(workspace) : nullptr;
+    return run_quant<DT>(x, numel, q, scale, dynamic, part, tk, kMaxPartials, stream, sms);
 }
 
 template <int DT>
@@ -343,8 +401,10 @@ extern "C" int fp8_quant_per_row(const void *x, int x_dtype, int64_t rows, int64
 namespace fp8l {
 namespace {
 
-constexpr int kNoallocMaxPartials = 2048;  // partial maxima the array holds
-static __device__ __align__(256) float g_noalloc_partials[kNoallocMaxPartials];
+// 2048 partial maxima, then one ticket word that is zero between calls (zero
+// at load, and every call leaves it at zero)
+constexpr int kNoallocMaxPartials = 2048;
+static __device__ __align__(256) float g_noalloc_partials[kNoallocMaxPartials + 64];
 
 constexpr int kNoallocMaxDevices = 64;
 std::atomic<float *> g_noalloc_ptr[kNoallocMaxDevices];
@@ -371,24 +431,10 @@ int noalloc_scratch(float **out) {
 template <int DT>
 int run_noalloc(const void *x, int64_t numel, uint8_t *q, float *scale, float *part,
                 cudaStream_t stream, int sms) {
-    const int64_t n_chunks = numel / kChunk;
-    int n_part = 0;
-    if (numel > 0) {
-        // every block writes its own partial and the cast kernel reads exactly
-        // the n_part entries this call wrote, so nothing needs clearing
-        int64_t blocks = (n_chunks + 2 * kThreads - 1) / (2 * kThreads);
-        if (blocks < 1) blocks = 1;
-        if (blocks > int64_t(sms) * 8) blocks = int64_t(sms) * 8;
-        if (blocks > kNoallocMaxPartials) blocks = kNoallocMaxPartials;
-        n_part = static_cast<int>(blocks);
-        absmax_kernel<DT><<<n_part, kThreads, 0, stream>>>(x, numel, part);
-        if (launch_status() != FP8L_OK) return FP8L_ECUDA;
-    }
-    const int64_t need = (n_chunks + kThreads - 1) / kThreads;
-    const int64_t cap = int64_t(sms) * 8;
-    const int cast_blocks = static_cast<int>(need < 1 ? 1 : (need < cap ? need : cap));
-    cast_kernel<DT, true><<<cast_blocks, kThreads, 0, stream>>>(x, numel, q, scale, part, n_part);
-    return launch_status();
+    // each block writes its own partial and the last block reads exactly the
+    // partials this call wrote; only the ticket word must start at zero
+    unsigned *tk = reinterpret_cast<unsigned *>(part + kNoallocMaxPartials);
+    return run_quant<DT>(x, numel, q, scale, true, part, tk, kNoallocMaxPartials, stream, sms);
 }
 
 }  // namespace

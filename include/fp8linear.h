@@ -80,8 +80,9 @@ enum fp8l_dtype {
  * and fp8_scaled_mm need.  The caller allocates it once (device memory,
  * 16-byte aligned), fills it with zeros once, and may reuse it for every
  * later call on streams that do not run those calls concurrently.  It holds
- * a device status word and the per-block partial maxima of the dynamic
- * quantizer; the library keeps nothing else in it between calls. */
+ * a device status word, the dynamic quantizer's ticket counter (zero
+ * between calls) and its per-block partial maxima; the library keeps nothing
+ * else in it between calls. */
 FP8L_API size_t fp8l_workspace_bytes(void);
 
 /* Per-tensor quantization of a [rows, cols] activation or weight tensor
@@ -169,15 +170,17 @@ FP8L_API int fp8_w8a16_mm(const void *x, int x_dtype, const uint8_t *w,
  * same scale, bit for bit), with the same arguments minus `dynamic` and
  * `workspace`.
  *
- * Scratch: the per-block partial maxima live in an 8 KiB array inside the
- * library image (2048 floats), which every GPU that loads the library holds
- * until the process exits.  A call never needs more than those 2048 entries,
- * so every size fp8_quant_per_tensor accepts is accepted here; rows*cols
- * above 2^40 is rejected with FP8L_ESHAPE.  Every call on a device shares
- * that one array: calls whose kernels may overlap on the GPU (different
- * streams without ordering between them) race on it and must not be issued.
- * Nothing in the array needs to start at zero; each call writes the entries
- * it reads.
+ * Scratch: the per-block partial maxima and a ticket counter live in an
+ * array of 2048 + 64 floats (8448 bytes) inside the library image, which
+ * every GPU that loads the library holds until the process exits.  A call
+ * never needs more than those 2048 partial entries, so every size
+ * fp8_quant_per_tensor accepts is accepted here; rows*cols above 2^40 is
+ * rejected with FP8L_ESHAPE.  Every call on a device shares that one array:
+ * calls whose kernels may overlap on the GPU (different streams without
+ * ordering between them) race on it and must not be issued.  Only the
+ * ticket counter must start at zero: it is zero when the library loads and
+ * every completed call leaves it at zero; each call writes the partial
+ * entries it reads.
  *
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and keeps it; make that
