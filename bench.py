@@ -62,7 +62,7 @@ FP8_OVER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor rate ratio (4.5 / 2.25 PF
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--steps", type=int, default=3000)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="decode_w8a16", choices=sorted(synthetic.WORKLOADS))
@@ -121,7 +121,7 @@ def barrier(world: int):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 50 ms."""
+    """nvidia-smi clocks / throttle reasons sampled every 25 ms."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -144,7 +144,7 @@ class ClockSampler:
 
     def start(self):
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-               "-lms", "50"]
+               "-lms", "25"]
         if self.gpu:
             cmd += ["-i", self.gpu]
         try:
@@ -296,7 +296,8 @@ class Workload:
             M, N, K = it["M"], it["N"], it["K"]
             if wl.kind == "w8a16":
                 out.append(Call("w8a16_skinny",
-                                lambda it=it: fl.fp8_w8a16_mm(it["x"], it["qw"], it["sw"], y=it["y"]),
+                                lambda it=it: fl.fp8_w8a16_mm(it["x"], it["qw"], it["sw"], y=it["y"],
+                                                              stable_weights=True),
                                 w8a16_bytes(M, N, K), "bytes", 1, (M, N, K)))
                 continue
             dynamic = wl.act_scale == "dynamic"
@@ -311,7 +312,7 @@ class Workload:
                             lambda it=it: fl.fp8_scaled_mm(it["qa"], it["qw"], it["sa"], it["sw"],
                                                            out_dtype=it["y"].dtype,
                                                            out_scale=it.get("os"), y=it["y"],
-                                                           ws=ws),
+                                                           ws=ws, stable_weights=True),
                             units, "bytes" if M <= 16 else "flops", 1, (M, N, K)))
         return out
 
@@ -345,13 +346,13 @@ class Workload:
             for it, x_host, y_host in zip(items, xh, yh):
                 it["x"].copy_(x_host, non_blocking=True)
                 if wl.kind == "w8a16":
-                    fl.fp8_w8a16_mm(it["x"], it["qw"], it["sw"], y=it["y"])
+                    fl.fp8_w8a16_mm(it["x"], it["qw"], it["sw"], y=it["y"], stable_weights=True)
                 else:
                     fl.fp8_quant_per_tensor(it["x"], q=it["qa"], scale=it["sa"],
                                             dynamic=wl.act_scale == "dynamic", ws=ws)
                     fl.fp8_scaled_mm(it["qa"], it["qw"], it["sa"], it["sw"],
                                      out_dtype=it["y"].dtype, out_scale=it.get("os"),
-                                     y=it["y"], ws=ws)
+                                     y=it["y"], ws=ws, stable_weights=True)
                 y_host.copy_(it["y"], non_blocking=True)
             stream.synchronize()
 
@@ -430,9 +431,11 @@ def _event(external):
 
 
 def measure(work: Workload, steps: int, warmup: int, world: int, sampler=None):
+    """Times `steps` replays of a CUDA graph of one step (no instrumentation
+    inside it), then replays a second graph of the same step with an event
+    node around every call to split the step time among the kernels."""
     dev = work.device
     stream = torch.cuda.Stream(device=dev)
-    graphs, evsets = [], []
     # eager pass: initializes the library (device check, shared-memory
     # attribute, TMA encoder) and the workspace outside any capture
     with torch.cuda.stream(stream):
@@ -440,22 +443,26 @@ def measure(work: Workload, steps: int, warmup: int, world: int, sampler=None):
             for c in work.calls(r):
                 c.fn()
     stream.synchronize()
+    graphs, inst, evsets, call_lists = [], [], [], []
     have_external = _event(True) is not None
-    call_lists = []
     for r in range(work.rot):
         calls = work.calls(r)
         call_lists.append(calls)
-        evs = [_event(True) for _ in range(len(calls) + 1)] if have_external else None
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for i, c in enumerate(calls):
-                if evs:
-                    evs[i].record()
+            for c in calls:
                 c.fn()
-            if evs:
-                evs[-1].record()
         graphs.append(g)
-        evsets.append(evs)
+        if have_external:
+            evs = [_event(True) for _ in range(len(calls) + 1)]
+            gi = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gi, stream=stream):
+                for i, c in enumerate(calls):
+                    evs[i].record()
+                    c.fn()
+                evs[-1].record()
+            inst.append(gi)
+            evsets.append(evs)
     torch.cuda.synchronize(dev)
 
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -478,51 +485,63 @@ def measure(work: Workload, steps: int, warmup: int, world: int, sampler=None):
     ms_total = start.elapsed_time(stop)
     ms_total = reduce_max(ms_total, world, dev)
 
-    # per-call durations from the in-graph event nodes of the last replay of
-    # each rotation copy
+    # per-call shares from the instrumented graphs (after the timed region)
     per_kind = {}
     if have_external:
-        for r in range(min(work.rot, steps)):
-            evs = evsets[r]
-            for i, c in enumerate(call_lists[r]):
-                d = evs[i].elapsed_time(evs[i + 1])
-                k = per_kind.setdefault(c.kind, {"ms": 0.0, "units": 0, "unit": c.unit, "calls": 0,
-                                                 "launches": 0})
-                k["ms"] += d
-                k["units"] += c.units
-                k["calls"] += 1
-                k["launches"] += c.launches
+        reps = max(3, min(20, steps))
+        with torch.cuda.stream(stream):
+            for rep in range(reps):
+                r = rep % work.rot
+                inst[r].replay()
+                stream.synchronize()
+                evs = evsets[r]
+                for i, c in enumerate(call_lists[r]):
+                    d = evs[i].elapsed_time(evs[i + 1])
+                    k = per_kind.setdefault(c.kind, {"ms": 0.0, "units": 0, "unit": c.unit,
+                                                     "calls": 0, "launches": 0})
+                    k["ms"] += d
+                    k["units"] += c.units
+                    k["calls"] += 1
+                    k["launches"] += c.launches
+        for k in per_kind.values():
+            k["units_per_step"] = k["units"] / reps
+            k["launches_per_step"] = k["launches"] / reps
     launches_per_step = sum(c.launches for c in call_lists[0])
     return {"ms_total": ms_total, "ms_per_step": ms_total / steps, "per_kind": per_kind,
-            "kernel_timing": "in-graph event nodes" if have_external else "none",
+            "kernel_timing": ("shares from event nodes in a separate replay of the step graph; "
+                              "kernel time = timed step time x share") if have_external else "none",
             "gpu_launches": launches_per_step * steps, "window": (tw0, t0, t1)}
 
 
-def roofline(per_kind, peaks, bound_override=None):
+def roofline(per_kind, peaks, ms_per_step):
+    """Roofline of the dominant kernel: its algorithmic units per step over
+    its time per step (the timed step time times its measured share)."""
     if not per_kind:
         return None, None
     total = sum(v["ms"] for v in per_kind.values())
     kind, v = max(per_kind.items(), key=lambda kv: kv[1]["ms"])
-    secs = v["ms"] / 1e3
+    share = v["ms"] / total if total > 0 else 1.0
+    secs = ms_per_step * share / 1e3
+    ups = v["units_per_step"]
     if v["unit"] == "flops":
-        achieved = v["units"] / secs / 1e12
+        achieved = ups / secs / 1e12
         peak = peaks["bf16_tflops"] * FP8_OVER_BF16
         rf = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1),
               "unit": "TFLOP/s", "frac": round(achieved / peak, 4)}
         rf["peak_source"] = (f"{peaks['source']} bf16 burst {peaks['bf16_tflops']} TFLOP/s x "
                              f"{FP8_OVER_BF16} (nominal FP8/BF16 dense ratio)")
     else:
-        achieved = v["units"] / secs / 1e9
+        achieved = ups / secs / 1e9
         peak = peaks["hbm_gbs"]
         rf = {"bound": "hbm", "achieved": round(achieved, 1), "peak": round(peak, 1),
               "unit": "GB/s", "frac": round(achieved / peak, 4)}
         rf["peak_source"] = f"{peaks['source']} HBM copy bandwidth"
     rf["kernel"] = kind
-    rf["share"] = round(v["ms"] / total, 4) if total > 0 else None
-    rf["launches_measured"] = v["launches"]
+    rf["share"] = round(share, 4)
+    rf["launches_per_step"] = v["launches_per_step"]
     rf["traffic"] = traffic_from_profile(kind)
-    return rf, {k: {"ms": round(x["ms"], 4), "share": round(x["ms"] / total, 4) if total else None,
-                    "calls": x["calls"], "launches": x["launches"]} for k, x in per_kind.items()}
+    return rf, {k: {"share": round(x["ms"] / total, 4) if total else None,
+                    "launches_per_step": x["launches_per_step"]} for k, x in per_kind.items()}
 
 
 KERNEL_SOURCES = {"w8a16_skinny": "skinny.cu", "scaled_mm_skinny": "skinny.cu",
@@ -568,7 +587,7 @@ def run_ours(args):
     b, f = work.step_units()
     unit = work.headline_unit()
     value = aggregate(b if unit == "GB/s" else f, res["ms_per_step"], world, unit)
-    rf, kinds = roofline(res["per_kind"], peaks)
+    rf, kinds = roofline(res["per_kind"], peaks, res["ms_per_step"])
     # end to end through the public API with host buffers
     e2e_steps = max(3, min(args.steps, 50))
     dt_e2e, h2d, d2h = work.e2e(e2e_steps)
@@ -617,7 +636,7 @@ def other_workloads(args, dev, peaks):
         res = measure(work, args.extra_steps, max(3, args.warmup // 2), 1)
         b, f = work.step_units()
         sec = res["ms_per_step"] / 1e3
-        rf, kinds = roofline(res["per_kind"], peaks)
+        rf, kinds = roofline(res["per_kind"], peaks, res["ms_per_step"])
         entry = {"workload": name, "value": round(f / sec / 1e12, 2), "unit": "TFLOP/s",
                  "ms_per_step": round(res["ms_per_step"], 4), "steps": args.extra_steps,
                  "roofline": rf, "kernels": kinds}

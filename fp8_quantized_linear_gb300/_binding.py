@@ -18,6 +18,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfp8linear.so")
 
 F16, BF16, E4M3, F32 = 0, 1, 2, 3
+WEIGHTS_STABLE = 1
 OK, EINVAL, ESHAPE, EALIGN, ECUDA, ETIMEOUT, EUNSUPPORTED = range(7)
 
 _DTYPE_CODE = {torch.float16: F16, torch.bfloat16: BF16, torch.float32: F32,
@@ -59,9 +60,9 @@ def load():
         lib.fp8_quant_per_row.restype = I
         lib.fp8_quant_per_row.argtypes = [P, I, I64, I64, P, P, P]
         lib.fp8_scaled_mm.restype = I
-        lib.fp8_scaled_mm.argtypes = [P, P, I64, I64, I64, P, P, I, P, P, I, P, P]
+        lib.fp8_scaled_mm.argtypes = [P, P, I64, I64, I64, P, P, I, P, P, I, P, ctypes.c_uint, P]
         lib.fp8_w8a16_mm.restype = I
-        lib.fp8_w8a16_mm.argtypes = [P, I, P, P, I64, I64, I64, P, P]
+        lib.fp8_w8a16_mm.argtypes = [P, I, P, P, I64, I64, I64, P, ctypes.c_uint, P]
         _lib = lib
         return lib
 
@@ -158,10 +159,11 @@ def fp8_quant_per_row(x: torch.Tensor, q: torch.Tensor | None = None,
 def fp8_scaled_mm(a: torch.Tensor, w: torch.Tensor, a_scale: torch.Tensor,
                   w_scale: torch.Tensor, out_dtype=torch.bfloat16,
                   out_scale: torch.Tensor | None = None, y: torch.Tensor | None = None,
-                  ws: torch.Tensor | None = None) -> torch.Tensor:
+                  ws: torch.Tensor | None = None, stable_weights: bool = False) -> torch.Tensor:
     """W8A8 product of E4M3 a [M, K] and w [N, K] with per-tensor a_scale and a
     per-tensor ([1]) or per-channel ([N]) w_scale.  out_dtype bf16 / fp16, or
-    uint8 (E4M3 codes, needs out_scale)."""
+    uint8 (E4M3 codes, needs out_scale).  stable_weights sets
+    FP8L_WEIGHTS_STABLE (no work in flight on the stream writes w or w_scale)."""
     _need_cuda(a, w, a_scale, w_scale, out_scale, y, ws)
     a, w = _codes(a), _codes(w)
     M, K = a.shape
@@ -182,15 +184,17 @@ def fp8_scaled_mm(a: torch.Tensor, w: torch.Tensor, a_scale: torch.Tensor,
         st = load().fp8_scaled_mm(
             a.data_ptr(), w.data_ptr(), M, N, K, a_scale.data_ptr(), w_scale.data_ptr(),
             per_channel, out_scale.data_ptr() if out_scale is not None else None,
-            _codes(y).data_ptr(), code, ws.data_ptr(), _stream(a.device))
+            _codes(y).data_ptr(), code, ws.data_ptr(), WEIGHTS_STABLE if stable_weights else 0,
+            _stream(a.device))
     _check(st, "fp8_scaled_mm")
     return y
 
 
 def fp8_w8a16_mm(x: torch.Tensor, w: torch.Tensor, w_scale: torch.Tensor,
-                 y: torch.Tensor | None = None) -> torch.Tensor:
+                 y: torch.Tensor | None = None, stable_weights: bool = False) -> torch.Tensor:
     """Weight-only product: fp16/bf16 x [M, K] times E4M3 w [N, K] with
-    per-channel w_scale [N]; the output has x's dtype."""
+    per-channel w_scale [N]; the output has x's dtype.  stable_weights sets
+    FP8L_WEIGHTS_STABLE (no work in flight on the stream writes w or w_scale)."""
     _need_cuda(x, w, w_scale, y)
     w = _codes(w)
     M, K = x.shape
@@ -201,6 +205,7 @@ def fp8_w8a16_mm(x: torch.Tensor, w: torch.Tensor, w_scale: torch.Tensor,
         y = torch.empty((M, N), dtype=x.dtype, device=x.device)
     with torch.cuda.device(x.device):
         st = load().fp8_w8a16_mm(x.data_ptr(), _DTYPE_CODE[x.dtype], w.data_ptr(),
-                                 w_scale.data_ptr(), M, N, K, y.data_ptr(), _stream(x.device))
+                                 w_scale.data_ptr(), M, N, K, y.data_ptr(),
+                                 WEIGHTS_STABLE if stable_weights else 0, _stream(x.device))
     _check(st, "fp8_w8a16_mm")
     return y

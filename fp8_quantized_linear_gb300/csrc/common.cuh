@@ -57,7 +57,8 @@ inline int launch_status() {
 // Launchers shared between translation units.
 int launch_skinny_e4m3(const uint8_t *a, const uint8_t *w, int M, int N, int K,
                        const float *a_scale, const float *w_scale, int w_per_channel,
-                       const float *out_scale, void *y, int out_dtype, cudaStream_t stream);
+                       const float *out_scale, void *y, int out_dtype, bool stable_weights,
+                       cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // device helpers

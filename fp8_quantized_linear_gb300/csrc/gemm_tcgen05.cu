@@ -490,10 +490,11 @@ int launch_tcgen05(const uint8_t *a, const uint8_t *w, int M, int N, int K, cons
 extern "C" int fp8_scaled_mm(const uint8_t *a, const uint8_t *w, int64_t M, int64_t N, int64_t K,
                              const float *a_scale, const float *w_scale, int w_per_channel,
                              const float *out_scale, void *y, int out_dtype, void *workspace,
-                             void *stream) {
+                             unsigned flags, void *stream) {
     using namespace fp8l;
     if (out_dtype != FP8L_F16 && out_dtype != FP8L_BF16 && out_dtype != FP8L_E4M3)
         return FP8L_EINVAL;
+    if ((flags & ~FP8L_WEIGHTS_STABLE) != 0u) return FP8L_EINVAL;
     if (a_scale == nullptr || w_scale == nullptr || workspace == nullptr || w == nullptr)
         return FP8L_EINVAL;
     if (out_dtype == FP8L_E4M3 && out_scale == nullptr) return FP8L_EINVAL;
@@ -515,7 +516,7 @@ extern "C" int fp8_scaled_mm(const uint8_t *a, const uint8_t *w, int64_t M, int6
     if (M <= 16)
         return launch_skinny_e4m3(a, w, static_cast<int>(M), static_cast<int>(N),
                                   static_cast<int>(K), a_scale, w_scale, pc, out_scale, y,
-                                  out_dtype, s);
+                                  out_dtype, (flags & FP8L_WEIGHTS_STABLE) != 0u, s);
     return launch_tcgen05(a, w, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
                           a_scale, w_scale, pc, out_scale, y, out_dtype, status_word(workspace),
                           sms, s);

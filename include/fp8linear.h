@@ -68,6 +68,17 @@ enum fp8l_status {
                              10.3, or the dtype combination is unsupported  */
 };
 
+/* Flags of the product entry points.
+ *
+ * FP8L_WEIGHTS_STABLE: the caller guarantees that no work still in flight on
+ * `stream` writes the weights `w` or the weight scales (the usual case of an
+ * inference loop, where weights are written once at load time).  The
+ * weight-streaming kernel is then launched as a programmatic dependent of
+ * the preceding kernel on the stream and issues its first weight loads
+ * before waiting for that kernel, so consecutive products overlap.
+ * Activations, scales and outputs are still only accessed after the wait. */
+#define FP8L_WEIGHTS_STABLE 1u
+
 /* Element types. */
 enum fp8l_dtype {
     FP8L_F16 = 0,   /* IEEE binary16                                         */
@@ -138,11 +149,12 @@ FP8L_API int fp8_quant_per_row(const void *x, int x_dtype, int64_t rows, int64_t
  * M >= 0 (M == 0 launches nothing); N and K are positive multiples of 16
  * (the FP8 GEMM shape rule), N, K <= 2^20, M <= 2^31 - 1.
  * M <= 16 runs a weight-streaming kernel; larger M runs the tcgen05 tensor
- * core kernel.  workspace: fp8l_workspace_bytes() bytes (status word). */
+ * core kernel.  workspace: fp8l_workspace_bytes() bytes (status word).
+ * flags: 0 or FP8L_WEIGHTS_STABLE (other bits are FP8L_EINVAL). */
 FP8L_API int fp8_scaled_mm(const uint8_t *a, const uint8_t *w, int64_t M, int64_t N,
                   int64_t K, const float *a_scale, const float *w_scale,
                   int w_per_channel, const float *out_scale, void *y,
-                  int out_dtype, void *workspace, void *stream);
+                  int out_dtype, void *workspace, unsigned flags, void *stream);
 
 /* W8A16 weight-only product ("Marlin fp8"): 16-bit activations times E4M3
  * weights with one scale per output channel.
@@ -154,10 +166,11 @@ FP8L_API int fp8_scaled_mm(const uint8_t *a, const uint8_t *w, int64_t M, int64_
  * w_scale: [N] floats; y: [M, N] of x_dtype.  M >= 0; N and K positive
  * multiples of 16, at most 2^20.  Built for decode batches (M <= 16); a
  * larger M is computed correctly in groups of 16 rows, each group
- * re-reading W. */
+ * re-reading W.  flags: 0 or FP8L_WEIGHTS_STABLE (other bits are
+ * FP8L_EINVAL). */
 FP8L_API int fp8_w8a16_mm(const void *x, int x_dtype, const uint8_t *w,
                  const float *w_scale, int64_t M, int64_t N, int64_t K,
-                 void *y, void *stream);
+                 void *y, unsigned flags, void *stream);
 
 /* Dynamic per-tensor quantization that allocates nothing and takes no
  * workspace.  The pages have no counterpart to this entry point.

@@ -68,13 +68,13 @@ def test_scaled_mm_argument_errors(lib):
     import fp8_quantized_linear_gb300._binding as b
     f = lib.fp8_scaled_mm
     ok = dict(a=A16, w=A16, M=32, N=32, K=32, sa=A16, sw=A16, pc=0, os=None, y=A16,
-              od=b.BF16, ws=A16, st=None)
+              od=b.BF16, ws=A16, fl=0, st=None)
 
     def call(**kw):
         d = dict(ok)
         d.update(kw)
         return f(d["a"], d["w"], d["M"], d["N"], d["K"], d["sa"], d["sw"], d["pc"], d["os"],
-                 d["y"], d["od"], d["ws"], d["st"])
+                 d["y"], d["od"], d["ws"], d["fl"], d["st"])
     assert call(od=7) == b.EINVAL
     assert call(sa=None) == b.EINVAL
     assert call(w=None) == b.EINVAL
@@ -89,17 +89,19 @@ def test_scaled_mm_argument_errors(lib):
     assert call(a=A16 + 8) == b.EALIGN
     assert call(y=A16 + 4) == b.EALIGN
     assert call(sw=A16 + 2) == b.EALIGN
+    assert call(fl=2) == b.EINVAL
 
 
 def test_w8a16_argument_errors(lib):
     import fp8_quantized_linear_gb300._binding as b
     f = lib.fp8_w8a16_mm
-    assert f(A16, b.E4M3, A16, A16, 1, 32, 32, A16, None) == b.EINVAL
-    assert f(A16, b.F32, A16, A16, 1, 32, 32, A16, None) == b.EINVAL
-    assert f(A16, b.F16, A16, A16, 1, 40, 32, A16, None) == b.ESHAPE
-    assert f(A16, b.F16, A16, A16, 1, 32, 40, A16, None) == b.ESHAPE
-    assert f(A16, b.F16, None, A16, 1, 32, 32, A16, None) == b.EINVAL
-    assert f(A16 + 2, b.F16, A16, A16, 1, 32, 32, A16, None) == b.EALIGN
+    assert f(A16, b.E4M3, A16, A16, 1, 32, 32, A16, 0, None) == b.EINVAL
+    assert f(A16, b.F32, A16, A16, 1, 32, 32, A16, 0, None) == b.EINVAL
+    assert f(A16, b.F16, A16, A16, 1, 32, 32, A16, 6, None) == b.EINVAL
+    assert f(A16, b.F16, A16, A16, 1, 40, 32, A16, 0, None) == b.ESHAPE
+    assert f(A16, b.F16, A16, A16, 1, 32, 40, A16, 0, None) == b.ESHAPE
+    assert f(A16, b.F16, None, A16, 1, 32, 32, A16, 0, None) == b.EINVAL
+    assert f(A16 + 2, b.F16, A16, A16, 1, 32, 32, A16, 0, None) == b.EALIGN
 
 
 def test_quant_argument_errors(lib):

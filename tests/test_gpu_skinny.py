@@ -116,3 +116,46 @@ def test_w8a8_small_m_exact_integer():
     exact = oracle.scaled_mm_bruteforce(qa, qw, np.float32(0.5), sw)
     want = torch.from_numpy(exact).to(torch.bfloat16).float().numpy()
     assert np.array_equal(y, want)
+
+
+@pytest.mark.parametrize("stable", [False, True])
+def test_w8a16_chain_with_stable_weights(stable):
+    # y1 = x W1^T, then y2 = y1 W2^T on the same stream: with
+    # FP8L_WEIGHTS_STABLE the second product starts before the first ends and
+    # must still read the finished y1
+    M, K, N1, N2 = 16, 4096, 4096, 4096
+    x = synthetic.activation(M, K, torch.float16, seed=71)
+    w1 = synthetic.weight(N1, K, torch.bfloat16, seed=72)
+    w2 = synthetic.weight(N2, N1, torch.bfloat16, seed=73)
+    q1, s1 = oracle.quant_per_row(w1)
+    q2, s2 = oracle.quant_per_row(w2)
+    q1d, s1d, q2d, s2d = dev(q1), dev(s1), dev(q2), dev(s2)
+    xd = dev(x)
+    for _ in range(3):
+        y1 = fl.fp8_w8a16_mm(xd, q1d, s1d, stable_weights=stable)
+        y2 = fl.fp8_w8a16_mm(y1, q2d, s2d, stable_weights=stable)
+    y1h = host(y1)
+    assert_gemm_close(y1h, oracle.w8a16_ref(x, q1, s1))
+    y1_f16 = torch.from_numpy(y1h).to(torch.float16)
+    assert_gemm_close(host(y2), oracle.w8a16_ref(y1_f16, q2, s2))
+
+
+def test_w8a8_small_m_chain_with_stable_weights():
+    # quantize -> product -> quantize its output -> product, all with the flag
+    M, K, N = 8, 4096, 4096
+    x = synthetic.activation(M, K, torch.bfloat16, seed=81)
+    w1 = synthetic.weight(N, K, torch.bfloat16, seed=82)
+    w2 = synthetic.weight(N, N, torch.bfloat16, seed=83)
+    q1, s1 = oracle.quant_per_row(w1)
+    q2, s2 = oracle.quant_per_row(w2)
+    qa, sa = fl.fp8_quant_per_tensor(dev(x))
+    y1 = fl.fp8_scaled_mm(qa, dev(q1), sa, dev(s1), out_dtype=torch.bfloat16, stable_weights=True)
+    qb, sb = fl.fp8_quant_per_tensor(y1)
+    y2 = fl.fp8_scaled_mm(qb, dev(q2), sb, dev(s2), out_dtype=torch.bfloat16, stable_weights=True)
+    qa_o, sa_o = oracle.quant_per_tensor(x)
+    assert np.array_equal(host(qa), qa_o)
+    assert_gemm_close(host(y1), oracle.scaled_mm_ref(qa_o, q1, sa_o, s1))
+    y1_bf16 = torch.from_numpy(host(y1)).to(torch.bfloat16)
+    qb_o, sb_o = oracle.quant_per_tensor(y1_bf16)
+    assert np.array_equal(host(qb), qb_o) and host(sb)[0] == sb_o
+    assert_gemm_close(host(y2), oracle.scaled_mm_ref(qb_o, q2, sb_o, s2))
