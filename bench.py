@@ -550,8 +550,9 @@ KERNEL_SOURCES = {"w8a16_skinny": "skinny.cu", "scaled_mm_skinny": "skinny.cu",
 
 
 def traffic_from_profile(kind):
-    """DRAM bytes per launch from the committed ncu summary of this kernel, if
-    the kernel source has not changed since that capture (else None)."""
+    """DRAM bytes of one captured launch of this kernel, from the committed ncu
+    summary, if the kernel source still has the hash the capture was taken
+    with (else None).  Returns {"bytes", "algorithmic_bytes", "launch"}."""
     src = KERNEL_SOURCES.get(kind)
     if src is None:
         return None
@@ -561,9 +562,10 @@ def traffic_from_profile(kind):
     h = hashlib.sha256(open(os.path.join(ROOT, "fp8_quantized_linear_gb300", "csrc", src),
                             "rb").read()).hexdigest()[:16]
     for line in open(path):
-        m = re.match(r"\|\s*(\w+)\s*\|\s*([0-9a-f]{16})\s*\|\s*([0-9.eE+]+)\s*\|", line)
-        if m and m.group(1) == kind and m.group(2) == h:
-            return float(m.group(3))
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) == 5 and cells[0] == kind and cells[1] == h:
+            return {"bytes": int(cells[2]), "algorithmic_bytes": int(cells[3]),
+                    "launch": cells[4]}
     return None
 
 
