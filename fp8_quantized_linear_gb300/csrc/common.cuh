@@ -12,7 +12,8 @@ namespace fp8l {
 // ---------------------------------------------------------------------------
 // Workspace layout (fp8l_workspace_bytes bytes, zero-filled by the caller once)
 //   [0, 4)                   uint32 status word (bit flags below)
-//   [4, 8)                   uint32 quantizer ticket counter (zero between calls)
+//   [4, 8)                   uint32 quantizer ticket / barrier counter (zero between calls)
+//   [8, 12)                  uint32 quantizer barrier generation (any value)
 //   [256, 256 + 4*kMaxParts) float per-block partial maxima of the quantizer
 constexpr size_t kStatusOffset = 0;
 constexpr size_t kPartialsOffset = 256;
@@ -39,6 +40,10 @@ inline unsigned *status_word(void *workspace) {
 
 inline unsigned *ticket_word(void *workspace) {
     return reinterpret_cast<unsigned *>(static_cast<char *>(workspace) + 4);
+}
+
+inline unsigned *gen_word(void *workspace) {
+    return reinterpret_cast<unsigned *>(static_cast<char *>(workspace) + 8);
 }
 
 inline float *partials(void *workspace) {

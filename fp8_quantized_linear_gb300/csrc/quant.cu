@@ -25,6 +25,8 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace fp8l {
@@ -320,9 +322,190 @@ int run_quant(const void *x, int64_t numel, uint8_t *q, float *scale, bool dynam
     return launch_status();
 }
 
+// ---------------------------------------------------------------------------
+// Single-pass dynamic quantization: one cooperative launch whose blocks are
+// all resident.  Each block owns a contiguous run of chunks; it loads them
+// (keeping them in shared memory when they fit), writes its partial maximum,
+// meets the other blocks at a grid barrier, reduces all partials to the same
+// scale, and casts its chunks from shared memory (or from a second read of X
+// when they did not fit).
+
+constexpr long long kBarrierCycles = 4LL << 30;  // ~2 s: a healthy barrier takes microseconds
+constexpr int kCacheBytes = 100 * 1024;          // per block; two blocks per SM
+
+// Grid barrier for a co-resident grid.  Thread 0 of every block arrives on
+// `count`; the last arrival resets it and advances `gen`; the others wait,
+// bounded, for `gen` to move.  Returns false after a time-out, which is
+// recorded in `status`.
+__device__ bool grid_barrier(unsigned *count, unsigned *gen, unsigned *status) {
+    __shared__ int ok_sh;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        volatile unsigned *vgen = gen;
+        const unsigned g0 = *vgen;
+        __threadfence();
+        if (atomicAdd(count, 1u) == gridDim.x - 1) {
+            *count = 0u;
+            __threadfence();
+            atomicAdd(gen, 1u);
+        } else {
+            const long long t0 = clock64();
+            while (*vgen == g0) {
+                if (clock64() - t0 > kBarrierCycles) {
+                    atomicOr(status, kStatusTimeout);
+                    ok = 0;
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+        __threadfence();
+        ok_sh = ok;
+    }
+    __syncthreads();
+    return ok_sh != 0;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads)
+quant_fused_kernel(const void *__restrict__ x, int64_t numel, uint8_t *__restrict__ q,
+                   float *__restrict__ scale, float *__restrict__ part, unsigned *count,
+                   unsigned *gen, unsigned *status, int64_t per, int64_t cache_chunks) {
+    extern __shared__ __align__(16) uint4 cache[];
+    __shared__ uint32_t red[33];
+    constexpr int V = Elt<DT>::kBytes;  // uint4 words per chunk
+    const uint4 *xv = static_cast<const uint4 *>(x);
+    uint4 *qv = reinterpret_cast<uint4 *>(q);
+    const int64_t n_chunks = numel / kChunk;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * per;
+    const int64_t c1 = c0 + per < n_chunks ? c0 + per : n_chunks;
+    const bool cached = c1 - c0 <= cache_chunks;
+
+    uint32_t m = 0;
+    int64_t c = c0 + threadIdx.x;
+    for (; c + 3 * kThreads < c1; c += 4 * kThreads) {
+        uint4 v[4][V];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) load_chunk<DT>(xv, c + u * kThreads, v[u]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            m = chunk_mag_max<DT>(v[u], m);
+            if (cached)
+#pragma unroll
+                for (int i = 0; i < V; ++i) cache[(c + u * kThreads - c0) * V + i] = v[u][i];
+        }
+    }
+    for (; c < c1; c += kThreads) {
+        uint4 v[V];
+        load_chunk<DT>(xv, c, v);
+        m = chunk_mag_max<DT>(v, m);
+        if (cached)
+#pragma unroll
+            for (int i = 0; i < V; ++i) cache[(c - c0) * V + i] = v[i];
+    }
+    m = fold_mag<DT>(m);
+    const int64_t tail = numel - n_chunks * kChunk;
+    if (blockIdx.x == 0 && threadIdx.x < tail)
+        m = max(m, scalar_mag_bits<DT>(x, n_chunks * kChunk + threadIdx.x));
+    m = block_max_u32(m, red);
+    if (threadIdx.x == 0) part[blockIdx.x] = mag_bits_to_float<DT>(m);
+
+    if (!grid_barrier(count, gen, status)) return;
+
+    uint32_t mm = 0;  // partials are non-negative floats: compare their bits
+    for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += kThreads)
+        mm = max(mm, __float_as_uint(__ldcg(part + i)));
+    mm = block_max_u32(mm, red);
+    const float s = scale_from_amax(__uint_as_float(mm));
+    if (blockIdx.x == 0 && threadIdx.x == 0) *scale = s;
+    const Divisor d(s);
+    for (c = c0 + threadIdx.x; c < c1; c += kThreads) {
+        uint4 v[V];
+        if (cached) {
+#pragma unroll
+            for (int i = 0; i < V; ++i) v[i] = cache[(c - c0) * V + i];
+        } else {
+            load_chunk<DT>(xv, c, v);
+        }
+        float f[kChunk];
+        chunk_values<DT>(v, f);
+        qv[c] = quant_chunk(f, d);
+    }
+    if (blockIdx.x == 0 && threadIdx.x < tail) {
+        const int64_t i = n_chunks * kChunk + threadIdx.x;
+        q[i] = e4m3(d(scalar_value<DT>(x, i)));
+    }
+}
+
+constexpr int kMaxDevicesQ = 64;
+std::atomic<int> g_fused_blocks[kMaxDevicesQ][4];  // co-resident blocks per SM, uncached
+
+template <int DT>
+int fused_blocks_per_sm_uncached() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesQ) return 0;
+    int nb = g_fused_blocks[dev][DT].load(std::memory_order_acquire);
+    if (nb == 0) {
+        if (cudaFuncSetAttribute(quant_fused_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kCacheBytes) != cudaSuccess)
+            return 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, quant_fused_kernel<DT>, kThreads, 0) !=
+                cudaSuccess ||
+            nb < 1)
+            return 0;
+        g_fused_blocks[dev][DT].store(nb, std::memory_order_release);
+    }
+    return nb;
+}
+
+template <int DT>
+int run_fused(const void *x, int64_t numel, uint8_t *q, float *scale, void *workspace,
+              cudaStream_t stream, int sms) {
+    const int nb = fused_blocks_per_sm_uncached<DT>();
+    if (nb == 0) return FP8L_ECUDA;
+    const int64_t n_chunks = numel / kChunk;
+    constexpr int64_t kChunkBytes = int64_t(kChunk) * Elt<DT>::kBytes;
+    // cached: two blocks per SM hold their whole run in shared memory
+    int64_t grid = int64_t(sms) * 2;
+    int64_t per = (n_chunks + grid - 1) / grid;
+    int64_t smem = per * kChunkBytes;
+    if (smem > kCacheBytes) {
+        // too large to keep on chip: as many resident blocks as fit, X read twice
+        grid = int64_t(sms) * nb;
+        if (grid > kMaxPartials) grid = kMaxPartials;
+        per = (n_chunks + grid - 1) / grid;
+        smem = 0;
+    }
+    // no more blocks than chunks need (at least one block)
+    const int64_t need = (n_chunks + kThreads - 1) / kThreads;
+    if (grid > need) {
+        grid = need < 1 ? 1 : need;
+        per = (n_chunks + grid - 1) / grid;
+        if (smem) smem = per * kChunkBytes;
+    }
+    const int64_t cache_chunks = smem / kChunkBytes;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, quant_fused_kernel<DT>, x, numel, q, scale, partials(workspace),
+                           ticket_word(workspace), gen_word(workspace),
+                           status_word(workspace), per, cache_chunks) != cudaSuccess)
+        return FP8L_ECUDA;
+    return launch_status();
+}
+
 template <int DT>
 int run_per_tensor(const void *x, int64_t numel, uint8_t *q, float *scale, bool dynamic,
                    void *workspace, cudaStream_t stream, int sms) {
+    if (dynamic && numel > 0) return run_fused<DT>(x, numel, q, scale, workspace, stream, sms);
     float *part = dynamic ? partials(workspace) : nullptr;
     unsigned *tk = dynamic ? ticket_word(workspace) : nullptr;
     return run_quant<DT>(x, numel, q, scale, dynamic, part, tk, kMaxPartials, stream, sms);

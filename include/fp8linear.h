@@ -91,9 +91,9 @@ enum fp8l_dtype {
  * and fp8_scaled_mm need.  The caller allocates it once (device memory,
  * 16-byte aligned), fills it with zeros once, and may reuse it for every
  * later call on streams that do not run those calls concurrently.  It holds
- * a device status word, the dynamic quantizer's ticket counter (zero
- * between calls) and its per-block partial maxima; the library keeps nothing
- * else in it between calls. */
+ * a device status word, the dynamic quantizer's barrier counter (zero
+ * between calls), its barrier generation word and its per-block partial
+ * maxima; the library keeps nothing else in it between calls. */
 FP8L_API size_t fp8l_workspace_bytes(void);
 
 /* Per-tensor quantization of a [rows, cols] activation or weight tensor

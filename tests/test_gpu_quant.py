@@ -142,3 +142,30 @@ def test_per_row_large():
     q_o, s_o = oracle.quant_per_row(w)
     assert np.array_equal(host(s), s_o)
     assert np.array_equal(host(q), q_o)
+
+
+@pytest.mark.parametrize("shape", [(1024, 4096), (8192, 4096)])
+def test_dynamic_inside_cuda_graph(shape):
+    # the single-pass quantizer is a cooperative launch: it must capture into
+    # a CUDA graph and give the oracle's bytes on every replay
+    M, K = shape
+    x = torch.empty((M, K), dtype=torch.bfloat16, device=DEV)
+    q = torch.empty((M, K), dtype=torch.uint8, device=DEV)
+    s = torch.empty(1, dtype=torch.float32, device=DEV)
+    ws = fl.workspace(DEV)
+    x.copy_(synthetic.activation(M, K, torch.bfloat16, seed=1).to(DEV))
+    fl.fp8_quant_per_tensor(x, q=q, scale=s, ws=ws)  # eager first call (set-up)
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fl.fp8_quant_per_tensor(x, q=q, scale=s, ws=ws)
+    for seed in (2, 3):
+        xs = synthetic.activation(M, K, torch.bfloat16, seed=seed, outlier_frac=0.01)
+        x.copy_(xs.to(DEV))
+        g.replay()
+        torch.cuda.synchronize()
+        q_o, s_o = oracle.quant_per_tensor(xs)
+        assert host(s)[0] == s_o
+        assert np.array_equal(host(q), q_o)
+    assert_status_ok()
