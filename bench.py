@@ -304,7 +304,7 @@ class Workload:
             out.append(Call("quant_dynamic" if dynamic else "quant_static",
                             lambda it=it, dyn=dynamic: fl.fp8_quant_per_tensor(
                                 it["x"], q=it["qa"], scale=it["sa"], dynamic=dyn, ws=ws),
-                            3 * M * K, "bytes", 2 if dynamic else 1, (M, N, K)))
+                            3 * M * K, "bytes", 1, (M, N, K)))
             kind = "scaled_mm_skinny" if M <= 16 else "scaled_mm_tcgen05"
             units = (w8a8_bytes(M, N, K, it["y"].element_size(), wl.w_scale == "channel")
                      if M <= 16 else 2 * M * N * K)

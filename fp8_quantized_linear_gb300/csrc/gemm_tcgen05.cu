@@ -66,6 +66,7 @@ struct GemmParams {
     void *y;
     int out_dtype;
     unsigned *status;
+    int split;  // > 1: a cluster of `split` CTAs shares one tile and splits its k-blocks
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -175,6 +176,29 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
         : "memory");
 }
 
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t local_addr, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(remote)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -250,6 +274,55 @@ __device__ __forceinline__ void store_row_chunk(const GemmParams &p, const uint3
     }
 }
 
+// Split mode: rows [rank*rows_per, ...) of the tile, summed over the cluster's
+// partial tiles (distributed shared memory), scaled, cast and stored; four
+// columns per thread, consecutive threads on consecutive columns.
+constexpr int kPartPitch = BN + 4;  // floats per partial-tile row (conflict-free v4 stores)
+static_assert(BM * kPartPitch * 4 <= STAGES * kStageBytes, "partial tile fits in the ring");
+
+__device__ void split_reduce_store(const GemmParams &p, int tile, int rank, uint32_t sbase) {
+    const int mb = tile % p.num_m_blocks;
+    const int nb = tile / p.num_m_blocks;
+    const int rows_per = (BM + p.split - 1) / p.split;
+    const int r0 = rank * rows_per;
+    const int r1 = r0 + rows_per < BM ? r0 + rows_per : BM;
+    const int items = (r1 - r0) * (BN / 4);
+    const float sa = __ldg(p.a_scale);
+    const float sw0 = __ldg(p.w_scale);
+    for (int i = threadIdx.x; i < items; i += blockDim.x) {
+        const int row = r0 + i / (BN / 4);
+        const int col = 4 * (i % (BN / 4));
+        const int m = mb * BM + row;
+        const int n = nb * BN + col;
+        if (m >= p.M || n >= p.N) continue;
+        const uint32_t off = sbase + static_cast<uint32_t>((row * kPartPitch + col) * 4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < p.split; ++q) {
+            const float4 v = ld_cluster_v4(off, static_cast<uint32_t>(q));
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        float v[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            v[j] *= sa * (p.w_per_channel ? __ldg(p.w_scale + n + j) : sw0);
+        if (p.out_dtype == FP8L_E4M3) {
+            const float os = __ldg(p.out_scale);
+            const uint32_t lo = e4m3x2(__fdiv_rn(v[0], os), __fdiv_rn(v[1], os));
+            const uint32_t hi = e4m3x2(__fdiv_rn(v[2], os), __fdiv_rn(v[3], os));
+            *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(p.y) + static_cast<size_t>(m) * p.N + n) =
+                lo | (hi << 16);
+        } else {
+            const uint32_t a = pack_out16(v[0], v[1], p.out_dtype);
+            const uint32_t b = pack_out16(v[2], v[3], p.out_dtype);
+            *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.y) + static_cast<size_t>(m) * p.N + n) =
+                make_uint2(a, b);
+        }
+    }
+}
+
 // ---------------------------------------------------------------- kernel
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -298,6 +371,18 @@ gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
     const uint32_t tmem_base = *tmem_slot;
 
     const int num_tiles = p.num_m_blocks * p.num_n_blocks;
+    // persistent mode: tiles blockIdx.x, +gridDim.x, ...; split mode: the
+    // cluster's one tile and this CTA's share of its k-blocks
+    const bool split = p.split > 1;
+    const int rank = split ? static_cast<int>(blockIdx.x) % p.split : 0;
+    const int tile_begin = split ? static_cast<int>(blockIdx.x) / p.split : static_cast<int>(blockIdx.x);
+    const int tile_step = split ? num_tiles : static_cast<int>(gridDim.x);
+    int kb_begin = 0, kb_end = p.num_k_blocks;
+    if (split) {
+        const int base = p.num_k_blocks / p.split, rem = p.num_k_blocks % p.split;
+        kb_begin = rank * base + (rank < rem ? rank : rem);
+        kb_end = kb_begin + base + (rank < rem ? 1 : 0);
+    }
 
     if (warp == 0) {
         if (lane == 0) {
@@ -307,10 +392,10 @@ gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
             uint32_t phase = 0;
             uint32_t issued = 0, issued_parity = 0;  // per stage: load in flight, its parity
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int tile = tile_begin; ok && tile < num_tiles; tile += tile_step) {
                 const int mb = tile % p.num_m_blocks;
                 const int nb = tile / p.num_m_blocks;
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
                         ok = false;
                         break;
@@ -339,11 +424,11 @@ gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int tile = tile_begin; ok && tile < num_tiles; tile += tile_step) {
                 if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) {
                         ok = false;
                         break;
@@ -354,7 +439,7 @@ gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k)
                         mma_f8(d_tmem, sw128_desc(sa + k * UMMA_K), sw128_desc(sb + k * UMMA_K),
-                               (kb | k) != 0 ? 1u : 0u);
+                               ((kb - kb_begin) | k) != 0 ? 1u : 0u);
                     mma_commit(empty_bar(stage));  // stage reusable once these MMAs retire
                     if (++stage == STAGES) {
                         stage = 0;
@@ -378,7 +463,26 @@ gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
         if (!p.w_per_channel) sa_sw = __ldg(p.a_scale) * __ldg(p.w_scale);
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        if (split) {
+            // fp32 partial tile into the (now idle) stage ring: part[row][col],
+            // row pitch kPartPitch floats
+            if (mbar_wait(tfull_bar(0), 0, abort_flag, p.status)) {
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+                const uint32_t prow = sbase + static_cast<uint32_t>(row * kPartPitch * 4);
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(taddr + static_cast<uint32_t>(c * 32), r);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(prow + static_cast<uint32_t>((c * 32 + 4 * j) * 4), r[4 * j],
+                                     r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+                }
+                tc_fence_before();
+            }
+        }
+        for (int tile = split ? num_tiles : tile_begin; tile < num_tiles; tile += tile_step) {
             const int mb = tile % p.num_m_blocks;
             const int nb = tile / p.num_m_blocks;
             if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status)) break;
@@ -399,6 +503,14 @@ gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
+    }
+
+    if (split) {
+        // every CTA of the cluster has its partial tile in shared memory; CTA
+        // `rank` adds the `split` partials of its rows and stores them
+        cluster_sync_all();
+        split_reduce_store(p, tile_begin, rank, sbase);
+        cluster_sync_all();  // peers may still be reading this CTA's partials
     }
 
     tc_fence_before();
@@ -479,8 +591,29 @@ int launch_tcgen05(const uint8_t *a, const uint8_t *w, int M, int N, int K, cons
     p.out_dtype = out_dtype;
     p.status = status;
     const int64_t tiles = int64_t(p.num_m_blocks) * p.num_n_blocks;
-    const int grid = static_cast<int>(tiles < sms ? tiles : sms);
-    gemm_f8_tcgen05<<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, p);
+    // Few tiles (small M): a cluster of `split` CTAs per tile splits K so
+    // that most SMs stream weights; otherwise one persistent CTA per SM.
+    int split = 1;
+    if (tiles * 2 <= sms) {
+        split = static_cast<int>(sms / tiles);
+        if (split > 8) split = 8;
+        if (split > p.num_k_blocks) split = p.num_k_blocks;
+        if (split < 1) split = 1;
+    }
+    p.split = split;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(split > 1 ? tiles * split : (tiles < sms ? tiles : sms)), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(split);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = split > 1 ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, gemm_f8_tcgen05, ma, mb, p) != cudaSuccess) return FP8L_ECUDA;
     return launch_status();
 }
 

@@ -382,27 +382,25 @@ quant_fused_kernel(const void *__restrict__ x, int64_t numel, uint8_t *__restric
     const int64_t c1 = c0 + per < n_chunks ? c0 + per : n_chunks;
     const bool cached = c1 - c0 <= cache_chunks;
 
+    // up to four chunks per thread requested at once (one round trip)
     uint32_t m = 0;
-    int64_t c = c0 + threadIdx.x;
-    for (; c + 3 * kThreads < c1; c += 4 * kThreads) {
+    int64_t c;
+    for (int64_t base = c0 + threadIdx.x; base < c1; base += 4 * kThreads) {
         uint4 v[4][V];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) load_chunk<DT>(xv, c + u * kThreads, v[u]);
+        for (int u = 0; u < 4; ++u) {
+            if (base + u * kThreads < c1) load_chunk<DT>(xv, base + u * kThreads, v[u]);
+        }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            m = chunk_mag_max<DT>(v[u], m);
-            if (cached)
+            const int64_t cu = base + u * kThreads;
+            if (cu < c1) {
+                m = chunk_mag_max<DT>(v[u], m);
+                if (cached)
 #pragma unroll
-                for (int i = 0; i < V; ++i) cache[(c + u * kThreads - c0) * V + i] = v[u][i];
+                    for (int i = 0; i < V; ++i) cache[(cu - c0) * V + i] = v[u][i];
+            }
         }
-    }
-    for (; c < c1; c += kThreads) {
-        uint4 v[V];
-        load_chunk<DT>(xv, c, v);
-        m = chunk_mag_max<DT>(v, m);
-        if (cached)
-#pragma unroll
-            for (int i = 0; i < V; ++i) cache[(c - c0) * V + i] = v[i];
     }
     m = fold_mag<DT>(m);
     const int64_t tail = numel - n_chunks * kChunk;

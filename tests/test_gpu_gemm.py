@@ -191,3 +191,20 @@ def test_zero_rows_launch_nothing():
     qw = torch.zeros((32, 64), dtype=torch.uint8, device=DEV)
     y = fl.fp8_scaled_mm(qa, qw, scalar(1.0), scalar(1.0))
     assert y.shape == (0, 32)
+
+
+@pytest.mark.parametrize("M,N,K", [(100, 512, 4096), (64, 4096, 4096), (128, 768, 1152)])
+def test_tcgen05_split_k_exact_integer(M, N, K):
+    # few output tiles: CTAs of a cluster split K and add their fp32 partial
+    # tiles through distributed shared memory; with exact-integer operands
+    # every partial and the total are exact, so the result is bit-exact
+    codes = np.array([0x40, 0x38, 0x30, 0x00, 0xB0, 0xB8, 0xC0], np.uint8)
+    rng = np.random.default_rng(M + N + K)
+    qa = codes[rng.integers(0, 7, (M, K))]
+    qw = codes[rng.integers(0, 7, (N, K))]
+    sw = np.array([2.0 ** (n % 5 - 2) for n in range(N)], np.float32)
+    y = host(fl.fp8_scaled_mm(dev(qa), dev(qw), scalar(0.5), dev(sw), out_dtype=torch.bfloat16))
+    exact = oracle.scaled_mm_ref(qa, qw, np.float32(0.5), sw)
+    want = torch.from_numpy(exact).to(torch.bfloat16).float().numpy()
+    assert np.array_equal(y, want)
+    assert_status_ok()
