@@ -12,9 +12,13 @@ namespace fp8l {
 // ---------------------------------------------------------------------------
 // Workspace layout (fp8l_workspace_bytes bytes, zero-filled by the caller once)
 //   [0, 4)                   uint32 status word (bit flags below)
-//   [4, 8)                   uint32 quantizer ticket / barrier counter (zero between calls)
-//   [8, 12)                  uint32 quantizer barrier generation (any value)
-//   [256, 256 + 4*kMaxParts) float per-block partial maxima of the quantizer
+//   [4, 8)                   uint32 two-launch quantizer ticket (zero between calls)
+//   [8, 12)                  uint32 single-launch quantizer call counter (any value)
+//   [16, 24)                 uint32[2] its grid-barrier arrival counts
+//   [24, 32)                 uint32[2] its maximum-magnitude words
+//                            (the pair of index `counter & 1` is zero when a
+//                            call starts; that call clears the other pair)
+//   [256, 256 + 4*kMaxParts) float per-block partial maxima (two-launch quantizer)
 constexpr size_t kStatusOffset = 0;
 constexpr size_t kPartialsOffset = 256;
 constexpr int kMaxPartials = 2048;
@@ -42,8 +46,16 @@ inline unsigned *ticket_word(void *workspace) {
     return reinterpret_cast<unsigned *>(static_cast<char *>(workspace) + 4);
 }
 
-inline unsigned *gen_word(void *workspace) {
+inline unsigned *epoch_word(void *workspace) {
     return reinterpret_cast<unsigned *>(static_cast<char *>(workspace) + 8);
+}
+
+inline unsigned *arrive_words(void *workspace) {
+    return reinterpret_cast<unsigned *>(static_cast<char *>(workspace) + 16);
+}
+
+inline unsigned *amax_words(void *workspace) {
+    return reinterpret_cast<unsigned *>(static_cast<char *>(workspace) + 24);
 }
 
 inline float *partials(void *workspace) {

@@ -91,9 +91,12 @@ enum fp8l_dtype {
  * and fp8_scaled_mm need.  The caller allocates it once (device memory,
  * 16-byte aligned), fills it with zeros once, and may reuse it for every
  * later call on streams that do not run those calls concurrently.  It holds
- * a device status word, the dynamic quantizer's barrier counter (zero
- * between calls), its barrier generation word and its per-block partial
- * maxima; the library keeps nothing else in it between calls. */
+ * a device status word and the dynamic quantizer's grid-barrier words (a call
+ * counter, two arrival counts and two maximum words used by alternate calls,
+ * and per-block partial maxima); the library keeps nothing else in it between
+ * calls.  After a call reports FP8L_ETIMEOUT (fp8l_read_status) the barrier
+ * words may be left mid-call: fill the workspace with zeros again before the
+ * next call. */
 FP8L_API size_t fp8l_workspace_bytes(void);
 
 /* Per-tensor quantization of a [rows, cols] activation or weight tensor

@@ -169,3 +169,43 @@ def test_dynamic_inside_cuda_graph(shape):
         assert host(s)[0] == s_o
         assert np.array_equal(host(q), q_o)
     assert_status_ok()
+
+
+def test_static_streamed_large():
+    # static scale on a tensor far larger than the on-chip stages: every
+    # piece is streamed once through the ring
+    x = synthetic.activation(8192, 4096, torch.bfloat16, seed=21)
+    q, _ = fl.fp8_quant_per_tensor(dev(x), scale=scalar(0.0371), dynamic=False)
+    q_o, _ = oracle.quant_per_tensor(x, scale=np.float32(0.0371))
+    assert np.array_equal(host(q), q_o)
+
+
+def test_dynamic_float32_streamed():
+    # 64 MB of fp32: pass 2 casts the resident pieces and re-reads the rest
+    _check_dynamic(synthetic.activation(4096, 4096, torch.float32, seed=22))
+
+
+@pytest.mark.parametrize("extra_words", [-1, 0, 1, 2049])
+def test_dynamic_resident_boundary(extra_words):
+    # one block per SM keeps 6 pieces of 2048 16-byte words on chip; these
+    # sizes put each block's run just under, at, and just over that
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    n_words = sms * (6 * 2048 + extra_words)
+    numel = n_words * 8 + 5  # bf16: 8 elements per word, plus a ragged tail
+    x = synthetic.activation(1, numel, torch.bfloat16, seed=23 + extra_words)
+    _check_dynamic(x)
+
+
+def test_alternating_grid_sizes_share_the_workspace():
+    # the barrier words alternate between calls; calls with 1 block and with
+    # one block per SM interleave on one workspace
+    ws = fl.workspace(DEV)
+    shapes = [(1, 16), (1024, 4096), (3, 33), (129, 4112), (1, 16), (2048, 4096), (16, 512)]
+    for rep in range(2):
+        for i, (M, K) in enumerate(shapes):
+            x = synthetic.activation(M, K, torch.bfloat16, seed=900 + 10 * rep + i)
+            q, s = fl.fp8_quant_per_tensor(dev(x), ws=ws)
+            q_o, s_o = oracle.quant_per_tensor(x)
+            assert host(s)[0] == s_o, (M, K)
+            assert np.array_equal(host(q), q_o), (M, K)
+    assert_status_ok()
