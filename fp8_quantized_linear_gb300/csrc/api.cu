@@ -1,5 +1,7 @@
 // Entry points that are not tied to one kernel: workspace size, status word,
-// error strings, device check.
+// error strings, device check; the tensor-map encoder of the TMA kernels.
+#include <cudaTypedefs.h>
+
 #include <atomic>
 
 #include "common.cuh"
@@ -32,6 +34,53 @@ int check_device(int *sm_count_out) {
     return state == 1 ? FP8L_OK : FP8L_EUNSUPPORTED;
 }
 
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> fn{nullptr};
+    PFN_cuTensorMapEncodeTiled_v12000 f = fn.load(std::memory_order_acquire);
+    if (f == nullptr) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        f = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        fn.store(f, std::memory_order_release);
+    }
+    return f;
+}
+}  // namespace
+
+int make_kmajor_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_k,
+                    int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (enc == nullptr) return FP8L_ECUDA;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_k), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8L_OK : FP8L_ECUDA;
+}
+
+namespace {
+// waits for `s`, reads the workspace status word at `dev`, clears it if set
+int read_and_clear(unsigned *dev, cudaStream_t s) {
+    unsigned host = 0;
+    if (cudaMemcpyAsync(&host, dev, sizeof(unsigned), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return FP8L_ECUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return FP8L_ECUDA;
+    if (host != 0u) {
+        if (cudaMemsetAsync(dev, 0, sizeof(unsigned), s) != cudaSuccess) return FP8L_ECUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return FP8L_ECUDA;
+    }
+    return (host & kStatusTimeout) ? FP8L_ETIMEOUT : FP8L_OK;
+}
+}  // namespace
+
 }  // namespace fp8l
 
 extern "C" {
@@ -56,17 +105,7 @@ const char *fp8l_strerror(int status) {
 int fp8l_read_status(void *workspace, void *stream) {
     if (workspace == nullptr) return FP8L_EINVAL;
     if (!fp8l::aligned16(workspace)) return FP8L_EALIGN;
-    cudaStream_t s = fp8l::as_stream(stream);
-    unsigned host = 0;
-    unsigned *dev = fp8l::status_word(workspace);
-    if (cudaMemcpyAsync(&host, dev, sizeof(unsigned), cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return FP8L_ECUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return FP8L_ECUDA;
-    if (host != 0u) {
-        if (cudaMemsetAsync(dev, 0, sizeof(unsigned), s) != cudaSuccess) return FP8L_ECUDA;
-        if (cudaStreamSynchronize(s) != cudaSuccess) return FP8L_ECUDA;
-    }
-    return (host & fp8l::kStatusTimeout) ? FP8L_ETIMEOUT : FP8L_OK;
+    return fp8l::read_and_clear(fp8l::status_word(workspace), fp8l::as_stream(stream));
 }
 
 }  // extern "C"

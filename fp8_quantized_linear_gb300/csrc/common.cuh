@@ -66,6 +66,11 @@ inline float *partials(void *workspace) {
 // answer and the SM count per device ordinal.
 int check_device(int *sm_count_out);
 
+// 2-D TMA map over a row-major [rows, K] byte matrix: box box_k x box_rows,
+// 128-byte swizzle, zero fill outside the matrix.
+int make_kmajor_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_k,
+                    int box_rows);
+
 // FP8L_ECUDA if the last launch failed, else FP8L_OK.
 inline int launch_status() {
     return cudaGetLastError() == cudaSuccess ? FP8L_OK : FP8L_ECUDA;

@@ -30,7 +30,6 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
-#include <cudaTypedefs.h>
 
 #include <atomic>
 
@@ -525,34 +524,9 @@ gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
 
 // ---------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> fn{nullptr};
-    PFN_cuTensorMapEncodeTiled_v12000 f = fn.load(std::memory_order_acquire);
-    if (f == nullptr) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        f = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-        fn.store(f, std::memory_order_release);
-    }
-    return f;
-}
-
 // 2-D map over a row-major [rows, K] uint8 matrix, box BK x box_rows, 128B swizzle
 int make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_rows) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-    if (enc == nullptr) return FP8L_ECUDA;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? FP8L_OK : FP8L_ECUDA;
+    return make_kmajor_map(map, ptr, rows, K, BK, box_rows);
 }
 
 constexpr int kMaxDevices = 64;

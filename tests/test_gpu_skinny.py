@@ -8,9 +8,16 @@ import torch
 import fp8_quantized_linear_gb300 as fl
 import oracle
 import synthetic
-from gpu_util import assert_e4m3_close, assert_gemm_close, dev, host, scalar
+from gpu_util import DEV, assert_e4m3_close, assert_gemm_close, assert_status_ok, dev, host, scalar
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _no_device_wait_gave_up():
+    # no bounded device-side wait of the calls made with the workspace gave up
+    yield
+    assert_status_ok()
 
 
 def _w8a16_case(M, N, K, xdtype, seed):
@@ -159,3 +166,37 @@ def test_w8a8_small_m_chain_with_stable_weights():
     qb_o, sb_o = oracle.quant_per_tensor(y1_bf16)
     assert np.array_equal(host(qb), qb_o) and host(sb)[0] == sb_o
     assert_gemm_close(host(y2), oracle.scaled_mm_ref(qb_o, q2, sb_o, s2))
+
+
+@pytest.mark.parametrize("M,N", [(1, 4096), (16, 4096), (4, 12288)])
+def test_w8a16_graph_replay_with_stable_weights(M, N):
+    # two chained products captured in one CUDA graph with the flag: the
+    # second is a programmatic dependent of the first (and, for N = 4096, a
+    # cluster launch that splits K); the graph must give the eager results
+    K = 4096
+    x = synthetic.activation(M, K, torch.float16, seed=91 + M)
+    w1 = synthetic.weight(N, K, torch.bfloat16, seed=92)
+    w2 = synthetic.weight(N, N, torch.bfloat16, seed=93)
+    q1, s1 = oracle.quant_per_row(w1)
+    q2, s2 = oracle.quant_per_row(w2)
+    q1d, s1d, q2d, s2d = dev(q1), dev(s1), dev(q2), dev(s2)
+    xd = dev(x)
+    y1 = torch.empty((M, N), dtype=torch.float16, device=DEV)
+    y2 = torch.empty((M, N), dtype=torch.float16, device=DEV)
+    fl.fp8_w8a16_mm(xd, q1d, s1d, y=y1, stable_weights=True)  # set-up outside the capture
+    fl.fp8_w8a16_mm(y1, q2d, s2d, y=y2, stable_weights=True)
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fl.fp8_w8a16_mm(xd, q1d, s1d, y=y1, stable_weights=True)
+        fl.fp8_w8a16_mm(y1, q2d, s2d, y=y2, stable_weights=True)
+    y1.zero_()
+    y2.zero_()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    y1h = host(y1)
+    assert_gemm_close(y1h, oracle.w8a16_ref(x, q1, s1))
+    assert_gemm_close(host(y2), oracle.w8a16_ref(torch.from_numpy(y1h).to(torch.float16), q2, s2))
