@@ -208,3 +208,21 @@ def test_tcgen05_split_k_exact_integer(M, N, K):
     want = torch.from_numpy(exact).to(torch.bfloat16).float().numpy()
     assert np.array_equal(y, want)
     assert_status_ok()
+
+
+@pytest.mark.parametrize("M,N,K", [(1024, 4096, 512), (1024, 11008, 256), (1000, 10240, 384),
+                                   (1024, 4112, 256), (1024, 57344, 128)])
+def test_tcgen05_prefill_shapes_exact_integer(M, N, K):
+    # persistent launches over the prefill and 70B widths, one with a
+    # 16-column tail in its last 256-column tile (N = 4112) and one with an M
+    # tail (M = 1000); exact-integer operands make the result bit-exact
+    codes = np.array([0x40, 0x38, 0x30, 0x00, 0xB0, 0xB8, 0xC0], np.uint8)
+    rng = np.random.default_rng(M + 3 * N + K)
+    qa = codes[rng.integers(0, 7, (M, K))]
+    qw = codes[rng.integers(0, 7, (N, K))]
+    sw = np.array([2.0 ** (n % 5 - 2) for n in range(N)], np.float32)
+    y = host(fl.fp8_scaled_mm(dev(qa), dev(qw), scalar(0.5), dev(sw), out_dtype=torch.bfloat16))
+    exact = oracle.scaled_mm_ref(qa, qw, np.float32(0.5), sw)
+    want = torch.from_numpy(exact).to(torch.bfloat16).float().numpy()
+    assert np.array_equal(y, want)
+    assert_status_ok()
