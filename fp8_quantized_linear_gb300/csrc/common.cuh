@@ -89,10 +89,12 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// 16-byte load that bypasses L1 (streamed weights).
+// 16-byte load of streamed weights: bypasses L1 and has L2 fetch the whole
+// 256-byte segment around it (the neighbouring chunks of the row are read by
+// other warps moments later).
 __device__ __forceinline__ uint4 ld_stream16(const void *p) {
     uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;

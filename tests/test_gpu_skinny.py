@@ -200,3 +200,17 @@ def test_w8a16_graph_replay_with_stable_weights(M, N):
     y1h = host(y1)
     assert_gemm_close(y1h, oracle.w8a16_ref(x, q1, s1))
     assert_gemm_close(host(y2), oracle.w8a16_ref(torch.from_numpy(y1h).to(torch.float16), q2, s2))
+
+
+@pytest.mark.parametrize("xdtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("M,N,K", [(16, 9728, 1024), (9, 12288, 512), (16, 22016, 320)])
+def test_w8a16_large_n_token_groups(M, N, K, xdtype):
+    # 9..16 tokens (two token tiles per CTA) over many channels; K = 320
+    # leaves a ragged last 64-k chunk
+    y, y_ref = _w8a16_case(M, N, K, xdtype, seed=M + N + K + 5)
+    assert_gemm_close(y, y_ref, (M, N, K, xdtype))
+
+
+@pytest.mark.parametrize("out", ["bf16", "e4m3"])
+def test_w8a8_small_m_large_n(out):
+    _w8a8_small(16, 10240, 1024, True, out, seed=123)
