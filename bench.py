@@ -549,6 +549,17 @@ KERNEL_SOURCES = {"w8a16_skinny": "skinny.cu", "scaled_mm_skinny": "skinny.cu",
                   "quant_static": "quant.cu"}
 
 
+def kernel_source_hash(src):
+    """sha256 prefix of a kernel's translation unit followed by the shared
+    header it includes (a change to either invalidates a capture)."""
+    csrc = os.path.join(ROOT, "fp8_quantized_linear_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in (src, "common.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_from_profile(kind):
     """DRAM bytes of one captured launch of this kernel, from the committed ncu
     summary, if the kernel source still has the hash the capture was taken
@@ -559,8 +570,7 @@ def traffic_from_profile(kind):
     path = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(path):
         return None
-    h = hashlib.sha256(open(os.path.join(ROOT, "fp8_quantized_linear_gb300", "csrc", src),
-                            "rb").read()).hexdigest()[:16]
+    h = kernel_source_hash(src)
     for line in open(path):
         cells = [c.strip() for c in line.strip().strip("|").split("|")]
         if len(cells) == 5 and cells[0] == kind and cells[1] == h:
