@@ -60,17 +60,36 @@ def test_w8a16_exact_integer_and_distinct_channel_scales():
     assert np.array_equal(y, want)
 
 
-def test_w8a16_permutation_weights():
-    # W is a permutation matrix: y[m, n] = sw[n] * x[m, pi(n)] exactly
-    K = N = 256
+@pytest.mark.parametrize("M,K", [(7, 256), (7, 208), (13, 256), (1, 1024), (8, 4096)])
+def test_w8a16_permutation_weights(M, K):
+    # W is a permutation matrix: y[m, n] = sw[n] * x[m, pi(n)] exactly, so a
+    # k position paired with the wrong weight byte anywhere in a chunk fails
+    # (K = 208: a ragged last chunk; 13 tokens: two token tiles).
+    N = K
     pi = (np.arange(N) * 37 + 11) % K
     qw = np.zeros((N, K), np.uint8)
     qw[np.arange(N), pi] = 0x38
     sw = np.array([2.0 ** (n % 5 - 2) for n in range(N)], np.float32)
-    x = synthetic.activation(7, K, torch.float16, seed=9)
+    x = synthetic.activation(M, K, torch.float16, seed=9 + M + K)
     y = host(fl.fp8_w8a16_mm(dev(x), dev(qw), dev(sw)))
     want = x.double().numpy()[:, pi] * sw[None, :]
     assert np.array_equal(y, want.astype(np.float16).astype(np.float32))
+
+
+@pytest.mark.parametrize("xdtype", [torch.float16, torch.bfloat16])
+def test_w8a16_activations_16_byte_aligned_only(xdtype):
+    # activations starting 16 bytes past a 32-byte boundary (the API asks
+    # for 16-byte alignment only)
+    M, N, K = 4, 256, 1024
+    x = synthetic.activation(M, K, xdtype, seed=31)
+    w = synthetic.weight(N, K, torch.bfloat16, seed=31)
+    qw, sw = oracle.quant_per_row(w)
+    buf = torch.empty(M * K + 8, dtype=xdtype, device=DEV)
+    xd = buf[8:].view(M, K)
+    xd.copy_(dev(x))
+    assert xd.data_ptr() % 32 == 16
+    y = host(fl.fp8_w8a16_mm(xd, dev(qw), dev(sw)))
+    assert_gemm_close(y, oracle.w8a16_ref(x, qw, sw), (M, N, K, xdtype))
 
 
 def test_w8a16_empty_batch():
@@ -109,13 +128,15 @@ def test_w8a8_small_m(M, N, K, per_channel, out):
     _w8a8_small(M, N, K, per_channel, out, seed=M + N + K)
 
 
-def test_w8a8_small_m_exact_integer():
+@pytest.mark.parametrize("M,K", [(16, 1024), (8, 1024), (3, 4096), (8, 1040)])
+def test_w8a8_small_m_exact_integer(M, K):
     # codes in {-2,-1,-0.5,0,0.5,1,2}: fp32 accumulation is exact; with
     # power-of-two scales the bf16 output equals the rounded exact value
+    # (one and two token tiles, K with and without a ragged last chunk)
     vals = {0x40: 2.0, 0x38: 1.0, 0x30: 0.5, 0x00: 0.0, 0xB0: -0.5, 0xB8: -1.0, 0xC0: -2.0}
     codes = np.array(list(vals), np.uint8)
-    rng = np.random.default_rng(12)
-    M, N, K = 16, 128, 1024
+    rng = np.random.default_rng(12 + M + K)
+    N = 128
     qa = codes[rng.integers(0, 7, (M, K))]
     qw = codes[rng.integers(0, 7, (N, K))]
     sw = np.array([2.0 ** -(n % 4) for n in range(N)], np.float32)
