@@ -14,7 +14,8 @@ shape of the workload:
     activation quantization (dynamic or static) plus the W8A8 product of
     every shape; metric TFLOP/s (2MNK), M <= 16 shapes also in GB/s.
 Weights are quantized once before timing (untimed setup), as the layer does
-after loading.  Each shape owns its own weight buffer and, where a step's
+after loading; W8A16 weights are then packed into the kernel's fragment
+order (--w8a16-layout row-major keeps [N, K] rows).  Each shape owns its own weight buffer and, where a step's
 footprint is below 3x the L2 size, the inputs rotate over several copies,
 so every timed step reads its operands from HBM.
 
@@ -69,6 +70,9 @@ def parse_args(argv=None):
     p.add_argument("--headline-only", action="store_true",
                    help="skip the other workloads' summary entries")
     p.add_argument("--extra-steps", type=int, default=20)
+    p.add_argument("--w8a16-layout", choices=["packed", "row-major"], default="packed",
+                   help="weights of the W8A16 products: packed once at setup into the "
+                        "kernel's fragment order (fp8_pack_w8a16_weights), or [N, K] rows")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
@@ -216,10 +220,11 @@ class Call:
 
 
 class Workload:
-    def __init__(self, name, device):
+    def __init__(self, name, device, packed_w8a16=True):
         import fp8_quantized_linear_gb300 as fl
         self.fl = fl
         self.name = name
+        self.packed = packed_w8a16 and synthetic.WORKLOADS[name].kind == "w8a16"
         self.wl = synthetic.WORKLOADS[name]
         self.device = device
         self.copies = []      # per rotation copy: list of per-shape dicts
@@ -253,6 +258,8 @@ class Workload:
             it = {"M": M, "N": N, "K": K, "x": x.to(dev)}
             if wl.kind == "w8a16":
                 it["qw"], it["sw"] = fl.fp8_quant_per_row(wbf)
+                if self.packed:
+                    it["qw"] = fl.fp8_pack_w8a16_weights(it["qw"])
                 it["y"] = torch.empty((M, N), dtype=wl.x_dtype, device=dev)
                 foot += w8a16_bytes(M, N, K)
             else:
@@ -297,7 +304,8 @@ class Workload:
             if wl.kind == "w8a16":
                 out.append(Call("w8a16_skinny",
                                 lambda it=it: fl.fp8_w8a16_mm(it["x"], it["qw"], it["sw"], y=it["y"],
-                                                              stable_weights=True),
+                                                              stable_weights=True,
+                                                              packed=self.packed),
                                 w8a16_bytes(M, N, K), "bytes", 1, (M, N, K)))
                 continue
             dynamic = wl.act_scale == "dynamic"
@@ -372,7 +380,8 @@ class Workload:
             x_dev.copy_(x_host, non_blocking=True)
             for it, x, y in zip(items, xs, ys):
                 if wl.kind == "w8a16":
-                    fl.fp8_w8a16_mm(x, it["qw"], it["sw"], y=y, stable_weights=True)
+                    fl.fp8_w8a16_mm(x, it["qw"], it["sw"], y=y, stable_weights=True,
+                                    packed=self.packed)
                 else:
                     fl.fp8_quant_per_tensor(x, q=it["qa"], scale=it["sa"],
                                             dynamic=wl.act_scale == "dynamic", ws=ws)
@@ -630,7 +639,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     peaks = load_peaks()
-    work = Workload(args.workload, dev)
+    work = Workload(args.workload, dev, packed_w8a16=args.w8a16_layout == "packed")
     work.build()
     sampler = ClockSampler(dev)
     sampler.start()
@@ -659,7 +668,11 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": (f"inputs larger than L2: {work.footprint / 2**20:.0f} MiB per step"
                           + (f" x {work.rot} rotating copies" if work.rot > 1 else "")),
-                   "graph": "one CUDA graph per step"},
+                   "graph": "one CUDA graph per step",
+                   **({"weights": ("E4M3 codes packed once at setup into the kernel's fragment "
+                                   "order (fp8_pack_w8a16_weights)" if work.packed
+                                   else "E4M3 codes as [N, K] rows")}
+                      if work.wl.kind == "w8a16" else {})},
         "roofline": rf, "kernels": kinds, "kernel_timing": res["kernel_timing"],
         "e2e": {"value": round(e2e_val, 3), "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,

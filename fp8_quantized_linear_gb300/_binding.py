@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libfp8linear.so")
 
 F16, BF16, E4M3, F32 = 0, 1, 2, 3
 WEIGHTS_STABLE = 1
+WEIGHTS_PACKED = 2
 OK, EINVAL, ESHAPE, EALIGN, ECUDA, ETIMEOUT, EUNSUPPORTED = range(7)
 
 _DTYPE_CODE = {torch.float16: F16, torch.bfloat16: BF16, torch.float32: F32,
@@ -63,6 +64,10 @@ def load():
         lib.fp8_scaled_mm.argtypes = [P, P, I64, I64, I64, P, P, I, P, P, I, P, ctypes.c_uint, P]
         lib.fp8_w8a16_mm.restype = I
         lib.fp8_w8a16_mm.argtypes = [P, I, P, P, I64, I64, I64, P, ctypes.c_uint, P]
+        lib.fp8_packed_weight_bytes.restype = ctypes.c_size_t
+        lib.fp8_packed_weight_bytes.argtypes = [I64, I64]
+        lib.fp8_pack_w8a16_weights.restype = I
+        lib.fp8_pack_w8a16_weights.argtypes = [P, I64, I64, P, P]
         _lib = lib
         return lib
 
@@ -190,22 +195,53 @@ def fp8_scaled_mm(a: torch.Tensor, w: torch.Tensor, a_scale: torch.Tensor,
     return y
 
 
+def fp8_packed_weight_bytes(N: int, K: int) -> int:
+    """Bytes of the packed layout of [N, K] E4M3 weights (0 for a bad shape)."""
+    return int(load().fp8_packed_weight_bytes(N, K))
+
+
+def fp8_pack_w8a16_weights(w: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """The packed copy of E4M3 weight codes w [N, K] that fp8_w8a16_mm reads
+    with packed=True: a 1-D uint8 tensor of fp8_packed_weight_bytes(N, K)."""
+    _need_cuda(w, out)
+    w = _codes(w)
+    N, K = w.shape
+    nbytes = fp8_packed_weight_bytes(N, K)
+    if nbytes == 0:
+        _check(ESHAPE, "fp8_pack_w8a16_weights")
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=w.device)
+    elif out.dtype != torch.uint8 or out.numel() != nbytes:
+        raise ValueError("out must be a uint8 tensor of fp8_packed_weight_bytes(N, K) elements")
+    with torch.cuda.device(w.device):
+        st = load().fp8_pack_w8a16_weights(w.data_ptr(), N, K, out.data_ptr(), _stream(w.device))
+    _check(st, "fp8_pack_w8a16_weights")
+    return out
+
+
 def fp8_w8a16_mm(x: torch.Tensor, w: torch.Tensor, w_scale: torch.Tensor,
-                 y: torch.Tensor | None = None, stable_weights: bool = False) -> torch.Tensor:
+                 y: torch.Tensor | None = None, stable_weights: bool = False,
+                 packed: bool = False) -> torch.Tensor:
     """Weight-only product: fp16/bf16 x [M, K] times E4M3 w [N, K] with
     per-channel w_scale [N]; the output has x's dtype.  stable_weights sets
-    FP8L_WEIGHTS_STABLE (no work in flight on the stream writes w or w_scale)."""
+    FP8L_WEIGHTS_STABLE (no work in flight on the stream writes w or
+    w_scale).  packed: w is the output of fp8_pack_w8a16_weights (N is
+    taken from w_scale) and FP8L_WEIGHTS_PACKED is set."""
     _need_cuda(x, w, w_scale, y)
     w = _codes(w)
     M, K = x.shape
-    N = w.shape[0]
-    if w.shape[1] != K or w_scale.numel() != N:
+    N = w_scale.numel()
+    if packed:
+        if w.dtype != torch.uint8 or w.numel() != fp8_packed_weight_bytes(N, K):
+            raise ValueError("packed weights must be fp8_pack_w8a16_weights output for [N, K]")
+    elif w.dim() != 2 or w.shape[0] != N or w.shape[1] != K:
         raise ValueError("shape mismatch")
     if y is None:
         y = torch.empty((M, N), dtype=x.dtype, device=x.device)
+    flags = (WEIGHTS_STABLE if stable_weights else 0) | (WEIGHTS_PACKED if packed else 0)
     with torch.cuda.device(x.device):
         st = load().fp8_w8a16_mm(x.data_ptr(), _DTYPE_CODE[x.dtype], w.data_ptr(),
-                                 w_scale.data_ptr(), M, N, K, y.data_ptr(),
-                                 WEIGHTS_STABLE if stable_weights else 0, _stream(x.device))
+                                 w_scale.data_ptr(), M, N, K, y.data_ptr(), flags,
+                                 _stream(x.device))
     _check(st, "fp8_w8a16_mm")
     return y

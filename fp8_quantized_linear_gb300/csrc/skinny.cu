@@ -23,6 +23,12 @@
 //     both byte pairs of a 32-bit word as 16-bit register halves; for bf16
 //     activations the f16 values are widened to bf16 (exact).  W8A8 uses the
 //     E4M3 x E4M3 tensor-core form directly (m16n8k32).
+//   * Packed weights (FP8L_WEIGHTS_PACKED): the [N, K] codes are permuted
+//     once at load time into the order the loads above consume them (the
+//     Marlin practice of packing weights to match the tensor-core fragments,
+//     "Condition to achieve linear speedup?").  Each CTA's 16 x K slab is
+//     then one contiguous block, and each warp load reads 512 contiguous
+//     bytes instead of 64 bytes from each of 8 rows.
 //   * With FP8L_WEIGHTS_STABLE the kernel is launched as a programmatic
 //     dependent of the preceding kernel on the stream: its first weight loads
 //     are issued before it waits for that kernel (griddepcontrol.wait), so
@@ -99,10 +105,36 @@ __device__ __forceinline__ void pdl_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Loads of data the preceding kernel on the stream may write (activations,
+// activation and output scales).  Coherent loads in volatile asm: they stay
+// after griddepcontrol.wait, and the non-coherent read-only path (whose
+// loads the compiler may treat as invariant and move ahead of the wait) is
+// only for data no kernel in flight writes, such as the stable weights.
+__device__ __forceinline__ uint4 ld_act16(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float ld_act_f32(const float *p) {
+    float v;
+    asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
 // Bytes of one token's activations per 64-element chunk: 128 (16-bit) or 64.
 template <int XK> struct XBytes { static constexpr int kPerLane = (XK == kXE4M3) ? 16 : 32; };
 
-template <int XK, int NT, int WARPS, int UNROLL>
+// Packed layout: 16-channel group G, 64-element chunk c (C = ceil(K / 64)
+// chunks per row) form the 1024-byte block at (G * C + c) * 1024; in it, the
+// 16 bytes of lane L = 4g + t for row 16G + g sit at 16L and those for row
+// 16G + g + 8 at 512 + 16L, covering k = 64c + 16t .. 64c + 16t + 15.  Bytes
+// with k >= K are zero.
+constexpr int kPackBlock = 1024;
+
+template <int XK, int NT, int WARPS, int UNROLL, bool PACKED>
 __global__ void __launch_bounds__(WARPS * 32, 2)
 skinny_kernel(const SkinnyArgs args) {
     constexpr int kXWords = XBytes<XK>::kPerLane / 4;  // 32-bit words per lane per token
@@ -122,8 +154,12 @@ skinny_kernel(const SkinnyArgs args) {
     const int M = args.M;
     const int nchunks = (K + 63) >> 6;
 
-    const uint8_t *w_g = args.w + static_cast<size_t>(n0 + g) * K + 16 * t4;
-    const uint8_t *w_g8 = w_g + static_cast<size_t>(8) * K;
+    // chunk c of rows g and g + 8: packed, the two halves of the 1024-byte
+    // block at w_g + c * 1024; row-major, w_g + 64c and w_g8 + 64c
+    const uint8_t *w_g =
+        PACKED ? args.w + static_cast<size_t>(blockIdx.x) * nchunks * kPackBlock + 16 * lane
+               : args.w + static_cast<size_t>(n0 + g) * K + 16 * t4;
+    const uint8_t *w_g8 = w_g + static_cast<size_t>(8) * K;  // row-major only
     const char *xbase = static_cast<const char *>(args.x);
     constexpr int kXElt = (XK == kXE4M3) ? 1 : 2;
 
@@ -141,8 +177,16 @@ skinny_kernel(const SkinnyArgs args) {
             const int c = c0 + u * WARPS;
             const int kk = c * 64 + 16 * t4;  // first k of this lane's 16
             const bool kin = (c < nchunks) && (kk < K);
-            wa[u] = kin ? ld_stream16(w_g + static_cast<size_t>(c) * 64) : make_uint4(0, 0, 0, 0);
-            wb[u] = kin ? ld_stream16(w_g8 + static_cast<size_t>(c) * 64) : make_uint4(0, 0, 0, 0);
+            if constexpr (PACKED) {
+                const uint8_t *wp = w_g + static_cast<size_t>(c) * kPackBlock;
+                wa[u] = kin ? ld_stream16(wp) : make_uint4(0, 0, 0, 0);
+                wb[u] = kin ? ld_stream16(wp + kPackBlock / 2) : make_uint4(0, 0, 0, 0);
+            } else {
+                wa[u] = kin ? ld_stream16(w_g + static_cast<size_t>(c) * 64)
+                            : make_uint4(0, 0, 0, 0);
+                wb[u] = kin ? ld_stream16(w_g8 + static_cast<size_t>(c) * 64)
+                            : make_uint4(0, 0, 0, 0);
+            }
             // everything but the weights may come from the preceding kernel:
             // wait for it once, after the first weight loads are in flight
             // (a no-op unless launched as a programmatic dependent)
@@ -155,7 +199,7 @@ skinny_kernel(const SkinnyArgs args) {
                     xbase + (static_cast<size_t>(m) * K + kk) * kXElt);
 #pragma unroll
                 for (int v = 0; v < kXWords / 4; ++v) {
-                    uint4 t = in ? __ldg(xp + v) : make_uint4(0, 0, 0, 0);
+                    uint4 t = in ? ld_act16(xp + v) : make_uint4(0, 0, 0, 0);
                     xw[u][nt][4 * v + 0] = t.x;
                     xw[u][nt][4 * v + 1] = t.y;
                     xw[u][nt][4 * v + 2] = t.z;
@@ -224,7 +268,7 @@ skinny_kernel(const SkinnyArgs args) {
         for (int wi = 0; wi < WARPS; ++wi) sum += red[wi][nt][r][lane_src];
         const int n = n0 + ch;
         float sc = args.w_per_channel ? __ldg(args.w_scale + n) : __ldg(args.w_scale);
-        if constexpr (XK == kXE4M3) sc *= __ldg(args.a_scale);
+        if constexpr (XK == kXE4M3) sc *= ld_act_f32(args.a_scale);
         const float v = sum * sc;
         const size_t yi = static_cast<size_t>(m) * args.N + n;
         if (args.out_dtype == FP8L_F16) {
@@ -232,7 +276,7 @@ skinny_kernel(const SkinnyArgs args) {
         } else if (args.out_dtype == FP8L_BF16) {
             static_cast<__nv_bfloat16 *>(args.y)[yi] = __float2bfloat16_rn(v);
         } else {
-            const float t = __fdiv_rn(v, __ldg(args.out_scale));
+            const float t = __fdiv_rn(v, ld_act_f32(args.out_scale));
             static_cast<uint8_t *>(args.y)[yi] = static_cast<uint8_t>(
                 __nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3));
         }
@@ -242,7 +286,7 @@ skinny_kernel(const SkinnyArgs args) {
 constexpr int kWarps = 16;
 constexpr int kUnroll = 2;
 
-template <int XK, int NT>
+template <int XK, int NT, bool PACKED>
 int launch_nt(const SkinnyArgs &a, bool stable_weights, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(a.N / 16), static_cast<unsigned>((a.M + 15) / 16), 1);
@@ -253,17 +297,37 @@ int launch_nt(const SkinnyArgs &a, bool stable_weights, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = stable_weights ? 1 : 0;
-    if (cudaLaunchKernelEx(&cfg, skinny_kernel<XK, NT, kWarps, kUnroll>, a) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, skinny_kernel<XK, NT, kWarps, kUnroll, PACKED>, a) != cudaSuccess)
         return FP8L_ECUDA;
     return launch_status();
 }
 
-template <int XK>
+template <int XK, bool PACKED = false>
 int launch(const SkinnyArgs &a, bool stable_weights, cudaStream_t stream) {
     if (a.M == 0) return FP8L_OK;
     const int tokens_in_group = a.M < 16 ? a.M : 16;
-    if (tokens_in_group <= 8) return launch_nt<XK, 1>(a, stable_weights, stream);
-    return launch_nt<XK, 2>(a, stable_weights, stream);
+    if (tokens_in_group <= 8) return launch_nt<XK, 1, PACKED>(a, stable_weights, stream);
+    return launch_nt<XK, 2, PACKED>(a, stable_weights, stream);
+}
+
+// One thread per 16 packed bytes: block (G, c), half h, lane L (see the
+// packed layout above).
+__global__ void pack_weights_kernel(const uint8_t *__restrict__ w, int N, int K, int nchunks,
+                                    uint8_t *__restrict__ wp) {
+    const size_t words = static_cast<size_t>(N / 16) * nchunks * (kPackBlock / 16);
+    for (size_t o = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; o < words;
+         o += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const int L = static_cast<int>(o & 31);
+        const int h = static_cast<int>((o >> 5) & 1);
+        const size_t blk = o >> 6;
+        const int c = static_cast<int>(blk % nchunks);
+        const size_t G = blk / nchunks;
+        const size_t row = G * 16 + 8 * h + (L >> 2);
+        const int k0 = 64 * c + 16 * (L & 3);
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (k0 < K) v = __ldg(reinterpret_cast<const uint4 *>(w + row * K + k0));
+        reinterpret_cast<uint4 *>(wp)[o] = v;
+    }
 }
 
 }  // namespace
@@ -278,12 +342,39 @@ int launch_skinny_e4m3(const uint8_t *a, const uint8_t *w, int M, int N, int K,
 
 }  // namespace fp8l
 
+extern "C" size_t fp8_packed_weight_bytes(int64_t N, int64_t K) {
+    if (N <= 0 || K <= 0 || N > (1 << 20) || K > (1 << 20) || N % 16 != 0 || K % 16 != 0)
+        return 0;
+    return static_cast<size_t>(N) * static_cast<size_t>((K + 63) / 64) * 64;
+}
+
+extern "C" int fp8_pack_w8a16_weights(const uint8_t *w, int64_t N, int64_t K, uint8_t *w_packed,
+                                      void *stream) {
+    using namespace fp8l;
+    if (fp8_packed_weight_bytes(N, K) == 0) return FP8L_ESHAPE;
+    if (w == nullptr || w_packed == nullptr) return FP8L_EINVAL;
+    if (!aligned16(w) || !aligned16(w_packed)) return FP8L_EALIGN;
+    int sms = 0;
+    int st = check_device(&sms);
+    if (st != FP8L_OK) return st;
+    const int nchunks = static_cast<int>((K + 63) / 64);
+    const size_t words = static_cast<size_t>(N / 16) * nchunks * (kPackBlock / 16);
+    const size_t want = (words + 255) / 256;
+    const unsigned blocks = static_cast<unsigned>(want < static_cast<size_t>(sms) * 8
+                                                      ? want
+                                                      : static_cast<size_t>(sms) * 8);
+    pack_weights_kernel<<<blocks, 256, 0, as_stream(stream)>>>(w, static_cast<int>(N),
+                                                               static_cast<int>(K), nchunks,
+                                                               w_packed);
+    return launch_status();
+}
+
 extern "C" int fp8_w8a16_mm(const void *x, int x_dtype, const uint8_t *w, const float *w_scale,
                             int64_t M, int64_t N, int64_t K, void *y, unsigned flags,
                             void *stream) {
     using namespace fp8l;
     if (x_dtype != FP8L_F16 && x_dtype != FP8L_BF16) return FP8L_EINVAL;
-    if ((flags & ~FP8L_WEIGHTS_STABLE) != 0u) return FP8L_EINVAL;
+    if ((flags & ~(FP8L_WEIGHTS_STABLE | FP8L_WEIGHTS_PACKED)) != 0u) return FP8L_EINVAL;
     if (M < 0 || M > 0x7FFFFFFF || N <= 0 || K <= 0 || N > (1 << 20) || K > (1 << 20) ||
         N % 16 != 0 || K % 16 != 0)
         return FP8L_ESHAPE;
@@ -297,6 +388,9 @@ extern "C" int fp8_w8a16_mm(const void *x, int x_dtype, const uint8_t *w, const 
     SkinnyArgs args{w, x, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
                     nullptr, w_scale, 1, nullptr, y, x_dtype};
     const bool stable = (flags & FP8L_WEIGHTS_STABLE) != 0u;
-    if (x_dtype == FP8L_F16) return launch<kXF16>(args, stable, as_stream(stream));
-    return launch<kXBF16>(args, stable, as_stream(stream));
+    const cudaStream_t s = as_stream(stream);
+    if ((flags & FP8L_WEIGHTS_PACKED) != 0u)
+        return x_dtype == FP8L_F16 ? launch<kXF16, true>(args, stable, s)
+                                   : launch<kXBF16, true>(args, stable, s);
+    return x_dtype == FP8L_F16 ? launch<kXF16>(args, stable, s) : launch<kXBF16>(args, stable, s);
 }

@@ -79,6 +79,10 @@ enum fp8l_status {
  * Activations, scales and outputs are still only accessed after the wait. */
 #define FP8L_WEIGHTS_STABLE 1u
 
+/* FP8L_WEIGHTS_PACKED (fp8_w8a16_mm only): `w` holds the weights in the
+ * packed layout written by fp8_pack_w8a16_weights, not as [N, K] rows. */
+#define FP8L_WEIGHTS_PACKED 2u
+
 /* Element types. */
 enum fp8l_dtype {
     FP8L_F16 = 0,   /* IEEE binary16                                         */
@@ -165,15 +169,41 @@ FP8L_API int fp8_scaled_mm(const uint8_t *a, const uint8_t *w, int64_t M, int64_
  *   y[m,n] = w_scale[n] * sum_k x[m,k] * dec(w[n,k])  (fp32 accumulation,
  *            rounded to nearest in x_dtype)
  *
- * x: [M, K] of x_dtype (FP8L_F16 or FP8L_BF16); w: [N, K] E4M3 codes;
+ * x: [M, K] of x_dtype (FP8L_F16 or FP8L_BF16); w: [N, K] E4M3 codes, or
+ * with FP8L_WEIGHTS_PACKED the packed layout of them
+ * (fp8_pack_w8a16_weights; the result is bit-for-bit the same);
  * w_scale: [N] floats; y: [M, N] of x_dtype.  M >= 0; N and K positive
  * multiples of 16, at most 2^20.  Built for decode batches (M <= 16); a
  * larger M is computed correctly in groups of 16 rows, each group
- * re-reading W.  flags: 0 or FP8L_WEIGHTS_STABLE (other bits are
- * FP8L_EINVAL). */
+ * re-reading W.  flags: any of FP8L_WEIGHTS_STABLE and FP8L_WEIGHTS_PACKED
+ * (other bits are FP8L_EINVAL). */
 FP8L_API int fp8_w8a16_mm(const void *x, int x_dtype, const uint8_t *w,
                  const float *w_scale, int64_t M, int64_t N, int64_t K,
                  void *y, unsigned flags, void *stream);
+
+/* Size in bytes of the packed layout of an [N, K] E4M3 weight tensor:
+ * N * ceil(K / 64) * 64.  Returns 0 when N or K is not a positive multiple
+ * of 16 at most 2^20. */
+FP8L_API size_t fp8_packed_weight_bytes(int64_t N, int64_t K);
+
+/* Repacks [N, K] E4M3 weight codes, once after they are loaded, into the
+ * order in which the W8A16 kernel reads them (Marlin-format weights are
+ * permuted at packing time to match the tensor-core mma fragments:
+ * "Condition to achieve linear speedup?").  fp8_w8a16_mm with
+ * FP8L_WEIGHTS_PACKED then reads each 16-channel group's weights as one
+ * contiguous block, 512 contiguous bytes per warp load.
+ *
+ * Layout, with C = ceil(K / 64): output channel n = 16G + 8h + g (g < 8,
+ * h < 2) and k = 64c + 16t + j (t < 4, j < 16) go to byte
+ *     (G * C + c) * 1024 + h * 512 + (4g + t) * 16 + j;
+ * bytes with k >= K are zero.
+ *
+ * w: [N, K] codes (16-byte aligned); w_packed: fp8_packed_weight_bytes(N, K)
+ * bytes (16-byte aligned, not overlapping w), written in full.  N and K are
+ * positive multiples of 16, at most 2^20.  Asynchronous on `stream`; the
+ * codes are only moved, never changed. */
+FP8L_API int fp8_pack_w8a16_weights(const uint8_t *w, int64_t N, int64_t K,
+                                    uint8_t *w_packed, void *stream);
 
 /* Dynamic per-tensor quantization that allocates nothing and takes no
  * workspace.  The pages have no counterpart to this entry point.

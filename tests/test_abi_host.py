@@ -29,6 +29,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for want in ("fp8_quant_per_tensor", "fp8_quant_per_row", "fp8_scaled_mm", "fp8_w8a16_mm",
+                 "fp8_pack_w8a16_weights", "fp8_packed_weight_bytes",
                  "fp8l_workspace_bytes", "fp8l_read_status", "fp8l_strerror", "fp8l_abi_version"):
         assert want in names
 
@@ -102,6 +103,27 @@ def test_w8a16_argument_errors(lib):
     assert f(A16, b.F16, A16, A16, 1, 32, 40, A16, 0, None) == b.ESHAPE
     assert f(A16, b.F16, None, A16, 1, 32, 32, A16, 0, None) == b.EINVAL
     assert f(A16 + 2, b.F16, A16, A16, 1, 32, 32, A16, 0, None) == b.EALIGN
+    assert f(A16, b.F16, A16, A16, 1, 32, 32, A16, 4, None) == b.EINVAL
+    assert f(A16, b.F16, A16, A16, 1, 32, 32, A16, b.WEIGHTS_PACKED | 8, None) == b.EINVAL
+
+
+def test_packed_weight_bytes_and_pack_argument_errors(lib):
+    import fp8_quantized_linear_gb300._binding as b
+    nb = lib.fp8_packed_weight_bytes
+    # N rows of ceil(K / 64) 64-byte chunks
+    assert nb(32, 4096) == 32 * 4096
+    assert nb(32, 208) == 32 * 256
+    assert nb(16, 16) == 16 * 64
+    assert nb(4096, 11008) == 4096 * 11008
+    for n, k in ((24, 64), (32, 0), (-16, 32), (32, 40), ((1 << 20) + 16, 64), (16, 1 << 21)):
+        assert nb(n, k) == 0, (n, k)
+    f = lib.fp8_pack_w8a16_weights
+    assert f(A16, 24, 64, A16, None) == b.ESHAPE
+    assert f(A16, 32, 40, A16, None) == b.ESHAPE
+    assert f(None, 32, 64, A16, None) == b.EINVAL
+    assert f(A16, 32, 64, None, None) == b.EINVAL
+    assert f(A16 + 8, 32, 64, A16, None) == b.EALIGN
+    assert f(A16, 32, 64, A16 + 4, None) == b.EALIGN
 
 
 def test_quant_argument_errors(lib):

@@ -189,6 +189,49 @@ def test_w8a8_small_m_chain_with_stable_weights():
     assert_gemm_close(host(y2), oracle.scaled_mm_ref(qb_o, q2, sb_o, s2))
 
 
+@pytest.mark.parametrize("M", [1, 8, 16])
+def test_w8a8_small_m_graph_replay_with_stable_weights(M):
+    # quantize -> product -> quantize -> product in one CUDA graph, the
+    # products launched as programmatic dependents: each reads codes and a
+    # scale the kernel before it writes.  Every intermediate is zeroed before
+    # each replay, so a read that ran ahead of its producer would show.
+    K = N = 4096
+    x = synthetic.activation(M, K, torch.bfloat16, seed=301 + M)
+    q1, s1 = oracle.quant_per_row(synthetic.weight(N, K, torch.bfloat16, seed=302))
+    q2, s2 = oracle.quant_per_row(synthetic.weight(N, N, torch.bfloat16, seed=303))
+    xd, q1d, s1d, q2d, s2d = dev(x), dev(q1), dev(s1), dev(q2), dev(s2)
+    ws = fl.workspace(DEV)
+    qa = torch.empty((M, K), dtype=torch.uint8, device=DEV)
+    qb = torch.empty((M, N), dtype=torch.uint8, device=DEV)
+    sa = torch.empty(1, dtype=torch.float32, device=DEV)
+    sb = torch.empty(1, dtype=torch.float32, device=DEV)
+    y1 = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    y2 = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+
+    def step():
+        fl.fp8_quant_per_tensor(xd, q=qa, scale=sa, ws=ws)
+        fl.fp8_scaled_mm(qa, q1d, sa, s1d, out_dtype=torch.bfloat16, y=y1, ws=ws,
+                         stable_weights=True)
+        fl.fp8_quant_per_tensor(y1, q=qb, scale=sb, ws=ws)
+        fl.fp8_scaled_mm(qb, q2d, sb, s2d, out_dtype=torch.bfloat16, y=y2, ws=ws,
+                         stable_weights=True)
+
+    step()
+    torch.cuda.synchronize()
+    want = y2.clone()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    for _ in range(3):
+        for t in (qa, qb, sa, sb, y1, y2):
+            t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y2, want)
+
+
 @pytest.mark.parametrize("M,N", [(1, 4096), (16, 4096), (4, 12288)])
 def test_w8a16_graph_replay_with_stable_weights(M, N):
     # two chained products captured in one CUDA graph with the flag: the
@@ -212,12 +255,15 @@ def test_w8a16_graph_replay_with_stable_weights(M, N):
     with torch.cuda.graph(g, stream=stream):
         fl.fp8_w8a16_mm(xd, q1d, s1d, y=y1, stable_weights=True)
         fl.fp8_w8a16_mm(y1, q2d, s2d, y=y2, stable_weights=True)
-    y1.zero_()
-    y2.zero_()
-    torch.cuda.synchronize()
+    want2 = fl.fp8_w8a16_mm(fl.fp8_w8a16_mm(xd, q1d, s1d), q2d, s2d)
     for _ in range(3):
+        # zeroed before every replay: a second product that read y1 before
+        # the first one finished writing it would see zeros
+        y1.zero_()
+        y2.zero_()
         g.replay()
-    torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        assert torch.equal(y2, want2)
     y1h = host(y1)
     assert_gemm_close(y1h, oracle.w8a16_ref(x, q1, s1))
     assert_gemm_close(host(y2), oracle.w8a16_ref(torch.from_numpy(y1h).to(torch.float16), q2, s2))
@@ -235,3 +281,98 @@ def test_w8a16_large_n_token_groups(M, N, K, xdtype):
 @pytest.mark.parametrize("out", ["bf16", "e4m3"])
 def test_w8a8_small_m_large_n(out):
     _w8a8_small(16, 10240, 1024, True, out, seed=123)
+
+
+def _packed_layout_reference(qw):
+    # the packed layout as the header states it: channel n = 16G + 8h + g,
+    # k = 64c + 16t + j go to byte (G*C + c)*1024 + h*512 + (4g + t)*16 + j,
+    # with zeros for k >= K
+    N, K = qw.shape
+    C = (K + 63) // 64
+    out = np.zeros(N * C * 64, np.uint8)
+    n = np.arange(N)[:, None]
+    k = np.arange(K)[None, :]
+    G, h, g = n // 16, (n % 16) // 8, n % 8
+    c, t, j = k // 64, (k % 64) // 16, k % 16
+    out[(G * C + c) * 1024 + h * 512 + (4 * g + t) * 16 + j] = qw
+    return out
+
+
+@pytest.mark.parametrize("N,K", [(16, 16), (32, 208), (48, 128), (64, 4096), (16, 11008)])
+def test_pack_weights_layout(N, K):
+    rng = np.random.default_rng(N + K)
+    qw = rng.integers(0, 256, (N, K), dtype=np.uint8)
+    packed = host(fl.fp8_pack_w8a16_weights(dev(qw)))
+    assert packed.dtype == np.uint8 and packed.size == fl.fp8_packed_weight_bytes(N, K)
+    assert np.array_equal(packed, _packed_layout_reference(qw))
+
+
+@pytest.mark.parametrize("xdtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("M,N,K", [(1, 16, 16), (3, 48, 208), (8, 256, 512), (9, 64, 1024),
+                                   (16, 272, 4096), (17, 64, 80), (40, 80, 144),
+                                   (16, 4096, 11008)])
+def test_w8a16_packed_weights_match_row_major(M, N, K, xdtype):
+    # the packed layout only moves the weight bytes: the product is the same
+    # bit for bit, and within tolerance of the oracle
+    x = synthetic.activation(M, K, xdtype, seed=M + N + K + 17)
+    w = synthetic.weight(N, K, torch.bfloat16, seed=M + N + K + 17)
+    qw, sw = oracle.quant_per_row(w)
+    xd, qwd, swd = dev(x), dev(qw), dev(sw)
+    y_rm = fl.fp8_w8a16_mm(xd, qwd, swd)
+    y_pk = fl.fp8_w8a16_mm(xd, fl.fp8_pack_w8a16_weights(qwd), swd, packed=True)
+    assert torch.equal(y_pk, y_rm)
+    assert_gemm_close(host(y_pk), oracle.w8a16_ref(x, qw, sw), (M, N, K, xdtype))
+
+
+@pytest.mark.parametrize("shape_idx", range(12))
+def test_w8a16_decode_workload_packed(shape_idx):
+    wl = synthetic.WORKLOADS["decode_w8a16"]
+    M, N, K = wl.shapes[shape_idx]
+    x = synthetic.activation(M, K, torch.float16, seed=wl.seed(shape_idx))
+    w = synthetic.weight(N, K, torch.bfloat16, seed=wl.seed(shape_idx))
+    qw, sw = oracle.quant_per_row(w)
+    y = fl.fp8_w8a16_mm(dev(x), fl.fp8_pack_w8a16_weights(dev(qw)), dev(sw), packed=True)
+    assert_gemm_close(host(y), oracle.w8a16_ref(x, qw, sw), (M, N, K))
+
+
+def test_w8a16_packed_permutation_weights():
+    # every (channel, k) position of the packed layout is paired with the
+    # right activation: y[m, n] = sw[n] * x[m, pi(n)] exactly
+    K = N = 208
+    pi = (np.arange(N) * 37 + 11) % K
+    qw = np.zeros((N, K), np.uint8)
+    qw[np.arange(N), pi] = 0x38
+    sw = np.array([2.0 ** (n % 5 - 2) for n in range(N)], np.float32)
+    x = synthetic.activation(13, K, torch.float16, seed=19)
+    y = host(fl.fp8_w8a16_mm(dev(x), fl.fp8_pack_w8a16_weights(dev(qw)), dev(sw), packed=True))
+    want = x.double().numpy()[:, pi] * sw[None, :]
+    assert np.array_equal(y, want.astype(np.float16).astype(np.float32))
+
+
+@pytest.mark.parametrize("M", [1, 16])
+def test_w8a16_packed_graph_replay_with_stable_weights(M):
+    # two dependent packed products in a CUDA graph, launched as programmatic
+    # dependents: the second reads the first one's output
+    K = N = 4096
+    x = synthetic.activation(M, K, torch.float16, seed=201 + M)
+    w1 = synthetic.weight(N, K, torch.bfloat16, seed=202)
+    w2 = synthetic.weight(N, K, torch.bfloat16, seed=203)
+    q1, s1 = oracle.quant_per_row(w1)
+    q2, s2 = oracle.quant_per_row(w2)
+    p1, p2 = fl.fp8_pack_w8a16_weights(dev(q1)), fl.fp8_pack_w8a16_weights(dev(q2))
+    s1d, s2d, xd = dev(s1), dev(s2), dev(x)
+    y1 = torch.empty((M, N), dtype=torch.float16, device=DEV)
+    y2 = torch.empty((M, N), dtype=torch.float16, device=DEV)
+    want = fl.fp8_w8a16_mm(fl.fp8_w8a16_mm(xd, dev(q1), s1d), dev(q2), s2d)
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fl.fp8_w8a16_mm(xd, p1, s1d, y=y1, stable_weights=True, packed=True)
+        fl.fp8_w8a16_mm(y1, p2, s2d, y=y2, stable_weights=True, packed=True)
+    for _ in range(3):
+        y1.zero_()
+        y2.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y2, want)
