@@ -1,0 +1,96 @@
+"""Host-side arithmetic of bench.py, checked without a GPU: the algorithmic
+bytes of one product, the whole-job aggregate over replicas, the roofline of
+the dominant kernel, and the DRAM-traffic lookup keyed on the kernel source
+(a capture counts only while the source it was taken from is unchanged)."""
+import os
+
+import pytest
+
+import bench
+
+
+def test_algorithmic_bytes_of_one_product():
+    # W8A16: fp16 X read (2MK), E4M3 W read (NK), fp16 Y written (2MN),
+    # one fp32 scale per channel (4N)
+    assert bench.w8a16_bytes(1, 16, 32) == 2 * 32 + 16 * 32 + 2 * 16 + 4 * 16
+    # the launch the committed M=16 capture was taken on
+    assert bench.w8a16_bytes(16, 22016, 4096) == 91101184
+    # W8A8: codes of A and W, the output, the weight scale(s), the activation scale
+    assert bench.w8a8_bytes(16, 32, 64, 2, True) == 16 * 64 + 32 * 64 + 16 * 32 * 2 + 4 * 32 + 4
+    assert bench.w8a8_bytes(16, 32, 64, 1, False) == 16 * 64 + 32 * 64 + 16 * 32 + 4 + 4
+
+
+def test_aggregate_is_the_work_of_all_replicas_over_the_slowest_step():
+    # 610 MB per step in 0.1 ms: 6100 GB/s on one GPU, 4x on four replicas
+    assert bench.aggregate(610e6, 0.1, 1, "GB/s") == pytest.approx(6100.0)
+    assert bench.aggregate(610e6, 0.1, 4, "GB/s") == pytest.approx(24400.0)
+    # 2e11 flops in 0.1 ms: 2000 TFLOP/s
+    assert bench.aggregate(2e11, 0.1, 1, "TFLOP/s") == pytest.approx(2000.0)
+
+
+PEAKS = {"hbm_gbs": 6807.9, "bf16_tflops": 1906.3, "source": "measured"}
+
+
+def test_roofline_of_the_dominant_kernel_uses_its_share_of_the_step():
+    per_kind = {
+        "quant_dynamic": {"ms": 1.0, "units_per_step": 12e6, "unit": "bytes",
+                          "launches_per_step": 2},
+        "scaled_mm_tcgen05": {"ms": 3.0, "units_per_step": 1.2e11, "unit": "flops",
+                              "launches_per_step": 2},
+    }
+    rf, kinds = bench.roofline(per_kind, PEAKS, ms_per_step=0.08)
+    assert rf["kernel"] == "scaled_mm_tcgen05"
+    assert rf["share"] == 0.75
+    # 1.2e11 flops in 0.08 ms x 0.75 = 60 us: 2000 TFLOP/s against 2 x 1906.3
+    assert rf["bound"] == "tensor" and rf["unit"] == "TFLOP/s"
+    assert rf["achieved"] == pytest.approx(2000.0, abs=0.01)
+    assert rf["peak"] == pytest.approx(3812.6)
+    assert rf["frac"] == pytest.approx(2000.0 / 3812.6, abs=1e-4)
+    assert kinds["quant_dynamic"]["share"] == 0.25
+
+
+def test_roofline_of_a_bandwidth_bound_step():
+    per_kind = {"w8a16_skinny": {"ms": 5.0, "units_per_step": 610e6, "unit": "bytes",
+                                 "launches_per_step": 12}}
+    rf, _ = bench.roofline(per_kind, PEAKS, ms_per_step=0.1265)
+    assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["share"] == 1.0
+    assert rf["achieved"] == pytest.approx(610e6 / 0.1265e-3 / 1e9, abs=0.1)
+    assert rf["peak"] == pytest.approx(6807.9)
+    assert rf["launches_per_step"] == 12
+
+
+def _fake_tree(root, skinny_src):
+    csrc = os.path.join(root, "fp8_quantized_linear_gb300", "csrc")
+    os.makedirs(csrc)
+    os.makedirs(os.path.join(root, "profiles"))
+    with open(os.path.join(csrc, "skinny.cu"), "w") as f:
+        f.write(skinny_src)
+    with open(os.path.join(csrc, "gemm_tcgen05.cu"), "w") as f:
+        f.write("// another kernel\n")
+    with open(os.path.join(csrc, "common.cuh"), "w") as f:
+        f.write("// shared header\n")
+
+
+def test_traffic_lookup_follows_the_kernel_source(tmp_path, monkeypatch):
+    root = str(tmp_path)
+    _fake_tree(root, "// kernel v1\n")
+    monkeypatch.setattr(bench, "ROOT", root)
+    h = bench.kernel_source_hash("skinny.cu")
+    with open(os.path.join(root, "profiles", "traffic.md"), "w") as f:
+        f.write("| kind | hash | bytes | algorithmic | launch |\n|---|---|---|---|---|\n")
+        f.write(f"| w8a16_skinny | {h} | 93158144 | 91101184 | M=16 N=22016 K=4096 |\n")
+    got = bench.traffic_from_profile("w8a16_skinny")
+    assert got == {"bytes": 93158144, "algorithmic_bytes": 91101184,
+                   "launch": "M=16 N=22016 K=4096"}
+    # a kind without a row has no figure
+    assert bench.traffic_from_profile("scaled_mm_tcgen05") is None
+    # a changed kernel source (or shared header) voids the capture
+    with open(os.path.join(root, "fp8_quantized_linear_gb300", "csrc", "skinny.cu"), "a") as f:
+        f.write("// edited\n")
+    assert bench.traffic_from_profile("w8a16_skinny") is None
+    with open(os.path.join(root, "fp8_quantized_linear_gb300", "csrc", "skinny.cu"), "w") as f:
+        f.write("// kernel v1\n")
+    assert bench.traffic_from_profile("w8a16_skinny") is not None
+    with open(os.path.join(root, "fp8_quantized_linear_gb300", "csrc", "common.cuh"), "a") as f:
+        f.write("// edited\n")
+    assert bench.traffic_from_profile("w8a16_skinny") is None
