@@ -21,6 +21,9 @@ What each function follows (page title, then the part of the page):
     (``b_scales`` of shape [1, N]).
   * static input / output scale: "RFC: FP8 Quantization Schema in vLLM",
     Interface Content, and the ``output_scale`` discussion after it.
+  * per-token activation scales (one per row of the activation codes): the
+    RFC's Scope, which leaves scales finer than per-tensor for later; read
+    as one scale per activation row.
 """
 from __future__ import annotations
 
@@ -80,6 +83,7 @@ def _load():
         lib.fp8o_quant_per_row.argtypes = [P, I64, I64, P, P]
         lib.fp8o_scaled_mm_f64.argtypes = [P, P, I64, I64, I64, ctypes.c_float,
                                            P, ctypes.c_int, P]
+        lib.fp8o_scaled_mm_rows_f64.argtypes = [P, P, I64, I64, I64, P, P, ctypes.c_int, P]
         lib.fp8o_w8a16_mm_f64.argtypes = [P, P, P, I64, I64, I64, P]
         _lib = lib
         return lib
@@ -191,17 +195,31 @@ def _scales(sw, N):
     return sw
 
 
+def _act_scales(sa, M):
+    sa = np.ascontiguousarray(np.asarray(sa, dtype=np.float32).reshape(-1))
+    if sa.size not in (1, M):
+        raise ValueError("activation scale must have 1 or M entries")
+    return sa
+
+
 def scaled_mm_bruteforce(qa, qw, sa, sw) -> np.ndarray:
-    """y = (sa * sw[n]) * sum_k dec(qa[m,k]) dec(qw[n,k]) by triple loop (C)."""
+    """y = (sa * sw[n]) * sum_k dec(qa[m,k]) dec(qw[n,k]) by triple loop (C).
+    sa is one per-tensor scale, or M per-row (per-token) scales sa[m]."""
     qa = np.ascontiguousarray(qa, dtype=np.uint8)
     qw = np.ascontiguousarray(qw, dtype=np.uint8)
     M, K = qa.shape
     N, K2 = qw.shape
     assert K == K2
     sw = _scales(sw, N)
+    sa = _act_scales(sa, M)
     y = np.empty((M, N), dtype=np.float64)
-    _load().fp8o_scaled_mm_f64(_ptr(qa), _ptr(qw), M, N, K, float(np.float32(sa)),
-                               _ptr(sw), int(sw.size == N and N != 1), _ptr(y))
+    per_channel = int(sw.size == N and N != 1)
+    if sa.size == 1:
+        _load().fp8o_scaled_mm_f64(_ptr(qa), _ptr(qw), M, N, K, float(sa[0]), _ptr(sw),
+                                   per_channel, _ptr(y))
+    else:
+        _load().fp8o_scaled_mm_rows_f64(_ptr(qa), _ptr(qw), M, N, K, _ptr(sa), _ptr(sw),
+                                        per_channel, _ptr(y))
     return y
 
 
@@ -213,8 +231,9 @@ def scaled_mm_ref(qa, qw, sa, sw) -> np.ndarray:
     W = table[np.asarray(qw, dtype=np.uint8)]
     N = W.shape[0]
     sw = _scales(sw, N).astype(np.float64)
+    sa = _act_scales(sa, A.shape[0]).astype(np.float64)
     acc = A @ W.T
-    return acc * (np.float64(np.float32(sa)) * sw.reshape(1, -1))
+    return acc * (sa.reshape(-1, 1) * sw.reshape(1, -1))
 
 
 def w8a16_bruteforce(x, qw, sw) -> np.ndarray:

@@ -189,6 +189,28 @@ void fp8o_scaled_mm_f64(const uint8_t *qa, const uint8_t *qw,
     }
 }
 
+/* The same product with one activation scale per row of qa (per token):
+ *   y[m,n] = (sa[m] * sw[n]) * sum_k dec(qa[m,k]) * dec(qw[n,k])
+ * The RFC (Scope) supports per-tensor scales and leaves per-channel and
+ * finer granularities for later; one scale per activation row is such a
+ * finer granularity on the activation side, the weight side unchanged.     */
+void fp8o_scaled_mm_rows_f64(const uint8_t *qa, const uint8_t *qw,
+                             int64_t M, int64_t N, int64_t K,
+                             const float *sa, const float *sw, int per_channel,
+                             double *y)
+{
+    const double *val = value_table();
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += val[qa[m * K + k]] * val[qw[n * K + k]];
+            double wscale = per_channel ? (double)sw[n] : (double)sw[0];
+            y[m * N + n] = ((double)sa[m] * wscale) * acc;
+        }
+    }
+}
+
 /* W8A16 weight-only product ("Marlin fp8"): 16-bit activations (passed here
  * already widened to fp32, which is exact) times FP8 weights with one scale
  * per output channel.

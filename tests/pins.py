@@ -256,6 +256,63 @@ def check_scaled_mm(mm, table: np.ndarray):
             assert y[m, n] == 0.75 * float(sw[n]) * acc4 / 4.0, (m, n)
 
 
+def check_scaled_mm_per_token(mm, table: np.ndarray):
+    """Pins of the product with one activation scale per row (per token):
+    y[m, n] = sa[m] * sw(n) * sum_k dec(qa[m,k]) dec(qw[n,k])."""
+    one = _code_of(table, 1.0)
+    # all-ones operands, distinct power-of-two row and column scales, M != N
+    # (a scale indexed by the column, or taken from one row, fails)
+    M, N, K = 5, 12, 24
+    qa = np.full((M, K), one, np.uint8)
+    qw = np.full((N, K), one, np.uint8)
+    sa = np.array([2.0 ** (m - 2) for m in range(M)], np.float32)
+    sw = np.array([2.0 ** (n % 7 - 3) for n in range(N)], np.float32)
+    y = mm(qa, qw, sa, sw)
+    assert y.shape == (M, N)
+    want = np.array([[K * 2.0 ** (m - 2) * 2.0 ** (n % 7 - 3) for n in range(N)]
+                     for m in range(M)])
+    assert np.array_equal(y, want), (y, want)
+    # per-tensor weight scale
+    y = mm(qa, qw, sa, np.array([3.0], np.float32))
+    assert np.array_equal(y, np.array([[K * 3.0 * 2.0 ** (m - 2)] * N for m in range(M)]))
+    # permutation weights: y[m, n] = sa[m] sw[n] dec(qa[m, pi(n)])
+    K = N = 16
+    pi = [(5 * n + 3) % K for n in range(N)]
+    rng = np.random.default_rng(11)
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    M = 6
+    qa = rng.choice(finite, size=(M, K)).astype(np.uint8)
+    qw = np.zeros((N, K), np.uint8)
+    for n in range(N):
+        qw[n, pi[n]] = one
+    sa = np.array([2.0 ** (-m) for m in range(M)], np.float32)
+    sw = np.array([2.0 ** (n % 5 - 2) for n in range(N)], np.float32)
+    y = mm(qa, qw, sa, sw)
+    want = np.array([[float(sa[m]) * float(sw[n]) * table[qa[m, pi[n]]] for n in range(N)]
+                     for m in range(M)])
+    assert np.array_equal(y, want)
+    # one scale for every row reduces to the per-tensor product
+    qa = rng.choice(finite, size=(4, 16)).astype(np.uint8)
+    qw = rng.choice(finite, size=(8, 16)).astype(np.uint8)
+    sw = np.array([2.0 ** -(n % 3) for n in range(8)], np.float32)
+    same = mm(qa, qw, np.full(4, 0.375, np.float32), sw)
+    assert np.array_equal(same, mm(qa, qw, np.float32(0.375), sw))
+    # exact integer arithmetic on codes in {-2,-1,-0.5,0,0.5,1,2}
+    vals = [-2.0, -1.0, -0.5, 0.0, 0.5, 1.0, 2.0]
+    codes = np.array([_code_of(table, v) for v in vals], np.uint8)
+    M, N, K = 7, 9, 33
+    ia = rng.integers(0, len(vals), size=(M, K))
+    iw = rng.integers(0, len(vals), size=(N, K))
+    sa = np.array([0.75 * 2.0 ** -(m % 4) for m in range(M)], np.float32)
+    sw = np.array([2.0 ** -(n % 3) for n in range(N)], np.float32)
+    y = mm(codes[ia], codes[iw], sa, sw)
+    twice = [int(2 * v) for v in vals]
+    for m in range(M):
+        for n in range(N):
+            acc4 = sum(twice[ia[m, k]] * twice[iw[n, k]] for k in range(K))
+            assert y[m, n] == float(sa[m]) * float(sw[n]) * acc4 / 4.0, (m, n)
+
+
 # ---------------------------------------------------------------------------
 # W8A16 product: ``fn(x_torch16, qw, sw) -> y float64 [M, N]``
 

@@ -23,6 +23,34 @@ def test_matmul_scaled_mm_pins(table):
     pins.check_scaled_mm(oracle.scaled_mm_ref, table)
 
 
+def test_bruteforce_scaled_mm_per_token_pins(table):
+    pins.check_scaled_mm_per_token(oracle.scaled_mm_bruteforce, table)
+
+
+def test_matmul_scaled_mm_per_token_pins(table):
+    pins.check_scaled_mm_per_token(oracle.scaled_mm_ref, table)
+
+
+@pytest.mark.parametrize("M,N,K", [(5, 48, 96), (17, 33, 80)])
+def test_per_token_matmul_path_equals_loops(M, N, K):
+    # per-token: one dynamic scale per activation row (the per-row quantizer)
+    x = synthetic.activation(M, K, torch.bfloat16, seed=M * 11 + K, outlier_frac=0.01)
+    qa, sa = oracle.quant_per_row(x)
+    qw, sw = oracle.quant_per_row(synthetic.weight(N, K, torch.bfloat16, seed=N + 1))
+    yb = oracle.scaled_mm_bruteforce(qa, qw, sa, sw)
+    ym = oracle.scaled_mm_ref(qa, qw, sa, sw)
+    assert np.allclose(ym, yb, rtol=1e-12, atol=1e-12 * np.abs(yb).max())
+
+
+def test_per_token_scales_must_match_the_rows():
+    qa = np.zeros((3, 16), np.uint8)
+    qw = np.zeros((4, 16), np.uint8)
+    with pytest.raises(ValueError):
+        oracle.scaled_mm_ref(qa, qw, np.ones(2, np.float32), np.ones(4, np.float32))
+    with pytest.raises(ValueError):
+        oracle.scaled_mm_bruteforce(qa, qw, np.ones(4, np.float32), np.ones(4, np.float32))
+
+
 def test_bruteforce_w8a16_pins(table):
     pins.check_w8a16(oracle.w8a16_bruteforce, table)
 

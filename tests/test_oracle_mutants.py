@@ -141,6 +141,37 @@ def test_scaled_mm_copy_without_mistake_passes(table):
     pins.check_scaled_mm(_mm_mutant(None, table), table)
 
 
+def _per_token_mutant(mistake, table):
+    def mm(qa, qw, sa, sw):
+        A = table[np.asarray(qa)]
+        W = table[np.asarray(qw)]
+        M, N = A.shape[0], W.shape[0]
+        sw = np.asarray(sw, np.float64).reshape(-1)
+        scale_n = np.full(N, sw[0]) if sw.size == 1 else sw
+        sa = np.asarray(sa, np.float64).reshape(-1)
+        rows = np.full(M, sa[0]) if sa.size == 1 else sa
+        scale = rows.reshape(-1, 1) * scale_n.reshape(1, -1)
+        if mistake == "scale_by_column":
+            # the row scale read at the column index: sa[n mod M]
+            scale = np.array([[rows[n % M] * scale_n[n] for n in range(N)] for _ in range(M)])
+        elif mistake == "first_row_scale":
+            scale = rows[0] * np.tile(scale_n, (M, 1))
+        elif mistake == "no_act_scale":
+            scale = np.tile(scale_n, (M, 1))
+        return (A @ W.T) * scale
+    return mm
+
+
+@pytest.mark.parametrize("mistake", ["scale_by_column", "first_row_scale", "no_act_scale"])
+def test_per_token_mutants_rejected(table, mistake):
+    with pytest.raises(AssertionError):
+        pins.check_scaled_mm_per_token(_per_token_mutant(mistake, table), table)
+
+
+def test_per_token_copy_without_mistake_passes(table):
+    pins.check_scaled_mm_per_token(_per_token_mutant(None, table), table)
+
+
 def _w8a16_mutant(mistake, table):
     def fn(x, qw, sw):
         X = oracle.widen(x).astype(np.float64)
