@@ -156,6 +156,25 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
         b.load()
 
 
+def test_cpu_tensors_are_refused_not_computed():
+    # there is no CPU fallback: every entry point wants CUDA tensors
+    import torch
+    import fp8_quantized_linear_gb300 as fl
+    x = torch.zeros((4, 32), dtype=torch.bfloat16)
+    q = torch.zeros((32, 32), dtype=torch.uint8)
+    one = torch.ones(1)
+    calls = [
+        lambda: fl.fp8_quant_per_tensor(x),
+        lambda: fl.fp8_quant_per_row(x),
+        lambda: fl.fp8_scaled_mm(q, q, one, one),
+        lambda: fl.fp8_w8a16_mm(x.half(), q, torch.ones(32)),
+        lambda: fl.fp8_pack_w8a16_weights(q),
+    ]
+    for call in calls:
+        with pytest.raises(TypeError, match="CUDA"):
+            call()
+
+
 def test_product_path_does_not_touch_the_oracle():
     pkg = os.path.join(ROOT, "fp8_quantized_linear_gb300")
     for dirpath, _, files in os.walk(pkg):
