@@ -17,6 +17,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfp8linear.so")
 
+ABI_VERSION = 2  # the library version this binding is written for
 F16, BF16, E4M3, F32 = 0, 1, 2, 3
 WEIGHTS_STABLE = 1
 WEIGHTS_PACKED = 2
@@ -49,9 +50,15 @@ def load():
                 f"g.build()\"` (nvcc, sm_103a)")
         lib = ctypes.CDLL(LIB_PATH)
         P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        lib.fp8l_abi_version.restype = I
+        lib.fp8l_abi_version.argtypes = []
+        version = lib.fp8l_abi_version()
+        if version != ABI_VERSION:
+            raise RuntimeError(
+                f"{LIB_PATH} has ABI version {version}, this binding needs {ABI_VERSION}: "
+                f"rebuild it with `python -c \"import __graft_entry__ as g; g.build()\"`")
         lib.fp8l_workspace_bytes.restype = ctypes.c_size_t
         lib.fp8l_workspace_bytes.argtypes = []
-        lib.fp8l_abi_version.restype = I
         lib.fp8l_strerror.restype = ctypes.c_char_p
         lib.fp8l_strerror.argtypes = [I]
         lib.fp8l_read_status.restype = I

@@ -46,7 +46,10 @@
 extern "C" {
 #endif
 
-#define FP8L_ABI_VERSION 1
+/* ABI version (fp8l_abi_version): 1, the first release; 2 adds
+ * fp8_pack_w8a16_weights, fp8_packed_weight_bytes and FP8L_WEIGHTS_PACKED.
+ * The change is additive: a caller written for version 1 runs unchanged. */
+#define FP8L_ABI_VERSION 2
 
 /* Only the entry points below are exported from the shared library. */
 #if defined(__GNUC__)

@@ -54,7 +54,7 @@ def test_only_c_abi_symbols_exported(lib):
 
 def test_constants(lib):
     import fp8_quantized_linear_gb300 as fl
-    assert lib.fp8l_abi_version() == 1
+    assert lib.fp8l_abi_version() == fl._binding.ABI_VERSION == 2
     assert fl.fp8l_workspace_bytes() >= 4096 and fl.fp8l_workspace_bytes() % 16 == 0
     for code in range(7):
         assert fl.strerror(code)
@@ -153,6 +153,28 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(b, "_lib", None)
     monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "nope.so"))
     with pytest.raises(RuntimeError, match="missing"):
+        b.load()
+
+
+def test_library_of_another_abi_version_is_refused(monkeypatch, tmp_path):
+    import fp8_quantized_linear_gb300._binding as b
+    stale = tmp_path / "libfp8linear.so"
+    stale.write_bytes(b"")
+
+    class OldLib:
+        class _Fn:
+            restype = None
+            argtypes = None
+
+            def __call__(self):
+                return 1
+
+        fp8l_abi_version = _Fn()
+
+    monkeypatch.setattr(b, "_lib", None)
+    monkeypatch.setattr(b, "LIB_PATH", str(stale))
+    monkeypatch.setattr(b.ctypes, "CDLL", lambda path: OldLib())
+    with pytest.raises(RuntimeError, match="ABI version 1"):
         b.load()
 
 
