@@ -776,11 +776,13 @@ def run_reference(args):
         tot_t += Workload.run_cpu_sample(jobs)
     val = (units * args.steps / tot_t / 1e9) if unit == "GB/s" else (units * args.steps / tot_t / 1e12)
     line = {"impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": unit,
-            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * tot_t / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
             "data": "synthetic (seeded)",
-            "config": {"workload": args.workload, "description": wl.description},
+            "config": {"workload": args.workload, "description": wl.description,
+                       "shapes": [list(sh) for sh in wl.shapes],
+                       "parallelism": "rank 0 only (host cores)"},
             "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": desc, "value": round(val, 6),
                              "unit": unit},
             "e2e": {"value": round(val, 6), "unit": unit, "h2d_bytes_per_step": 0,

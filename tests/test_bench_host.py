@@ -94,3 +94,25 @@ def test_traffic_lookup_follows_the_kernel_source(tmp_path, monkeypatch):
     with open(os.path.join(root, "fp8_quantized_linear_gb300", "csrc", "common.cuh"), "a") as f:
         f.write("// edited\n")
     assert bench.traffic_from_profile("w8a16_skinny") is None
+
+
+def test_reference_arm_prints_one_line_on_rank_0_only(monkeypatch, capsys):
+    # the oracle timed on the host: rank 0 prints the line, other ranks
+    # return without work
+    import json
+    args = bench.parse_args(["--impl", "reference", "--steps", "1", "--warmup", "3",
+                             "--workload", "tiny_w8a8"])
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+    bench.run_reference(args)
+    assert capsys.readouterr().out == ""
+    monkeypatch.setenv("RANK", "0")
+    bench.run_reference(args)
+    lines = capsys.readouterr().out.strip().splitlines()
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
+    assert line["unit"] == "TFLOP/s" and line["value"] > 0
+    assert line["config"]["workload"] == "tiny_w8a8"
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
