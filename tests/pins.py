@@ -355,3 +355,180 @@ def check_w8a16(fn, table: np.ndarray):
         for n in range(N):
             acc2 = sum(int(xi[m, k]) * twice[iw[n, k]] for k in range(K))
             assert y[m, n] == float(sw[n]) * acc2 / 2.0, (m, n)
+
+
+# ---------------------------------------------------------------------------
+# Parity criteria.  The GPU parity tests of every floating-point product go
+# through these acceptance functions, so they are pinned like the arithmetic:
+# hand-built (y, y_ref) pairs just inside and just outside each bound.
+
+def _ones_case(delta_one=0.0, delta_all=0.0, scale=1.0):
+    """y_ref = scale * ones(10, 10) (rms = scale, ||y_ref||_F = 10 scale);
+    y = y_ref with every element moved by delta_all * scale and element
+    (3, 4) moved further by delta_one * scale."""
+    y_ref = np.full((10, 10), scale, np.float64)
+    y = y_ref + delta_all * scale
+    y[3, 4] += delta_one * scale
+    return y, y_ref
+
+
+def check_gemm_close(close):
+    """``close(y, y_ref) -> {"ok": bool, ...}``: elementwise
+    |y - y_ref| <= 1e-2 (|y_ref| + rms(y_ref)) and relative Frobenius error
+    <= 5e-3, the bound built from the reference alone."""
+    for scale in (1.0, 1e3, 1e-3):
+        # identical outputs pass
+        y, r = _ones_case(scale=scale)
+        assert close(y, r)["ok"]
+        # one element at 0.95 of its bound (0.02 scale): the Frobenius error
+        # is 0.0019, so the elementwise bound alone decides
+        y, r = _ones_case(delta_one=0.019, scale=scale)
+        assert close(y, r)["ok"], scale
+        # ... and at 1.005 of it, upwards: a bound built from y (which has
+        # grown) instead of y_ref would admit this one
+        y, r = _ones_case(delta_one=0.0201, scale=scale)
+        assert not close(y, r)["ok"], scale
+        # every element moved by 0.00498 (elementwise ratio 0.25): Frobenius
+        # 0.00498 passes, 0.00502 fails; dividing by ||y|| instead of
+        # ||y_ref|| would pass the latter (0.004995)
+        y, r = _ones_case(delta_all=0.00498, scale=scale)
+        assert close(y, r)["ok"], scale
+        y, r = _ones_case(delta_all=0.00502, scale=scale)
+        assert not close(y, r)["ok"], scale
+        # the same error downwards
+        y, r = _ones_case(delta_all=-0.00502, scale=scale)
+        assert not close(y, r)["ok"], scale
+    # the elementwise bound has the rms term: an element whose reference is
+    # zero may be off by up to 1e-2 rms(y_ref)
+    y, r = _ones_case()
+    r[0, 0] = 0.0
+    rms = float(np.sqrt(np.mean(r ** 2)))
+    y[0, 0] = 0.0098 * rms
+    assert close(y, r)["ok"]
+    y[0, 0] = 0.0102 * rms
+    assert not close(y, r)["ok"]
+    # an all-zero reference admits only an all-zero output
+    z = np.zeros((4, 6))
+    assert close(z.copy(), z)["ok"]
+    y = z.copy()
+    y[2, 3] = 1e-30
+    assert not close(y, z)["ok"]
+    # non-finite outputs are rejected
+    for bad in (np.nan, np.inf, -np.inf):
+        y, r = _ones_case()
+        y[1, 1] = bad
+        assert not close(y, r)["ok"], bad
+    # empty outputs pass
+    assert close(np.zeros((0, 5)), np.zeros((0, 5)))["ok"]
+
+
+def brute_midpoint_distance(t, table: np.ndarray) -> np.ndarray:
+    """Independent restatement: the distance from min(|t|, 448) to the
+    nearest of the 126 midpoints between consecutive non-negative finite
+    E4M3 values, by a scan over all of them."""
+    pos = table[:127]
+    mids = [(pos[i] + pos[i + 1]) / 2 for i in range(126)]
+    out = []
+    for v in np.asarray(t, np.float64).reshape(-1):
+        a = min(abs(v), 448.0)
+        out.append(min(abs(a - m) for m in mids))
+    return np.array(out)
+
+
+def check_midpoint_distance(dist, table: np.ndarray):
+    """``dist(t) -> distance of each |t| (clipped to 448) to the nearest
+    rounding midpoint of E4M3``."""
+    # hand values: a midpoint itself; a code value (1.0 sits between the
+    # midpoints 0.96875 and 1.0625); zero (first midpoint 2^-10); beyond the
+    # largest value (clipped to 448, the last midpoint is 432); the sign
+    t = np.array([1.0625, 1.0, -1.0, 0.0, 2.0 ** -10, 500.0, 448.0, -3.0 * 2.0 ** -10])
+    want = np.array([0.0, 0.03125, 0.03125, 2.0 ** -10, 0.0, 16.0, 16.0, 0.0])
+    got = np.asarray(dist(t), np.float64)
+    assert np.array_equal(got, want), (got, want)
+    # against the scan on every code value, every midpoint, and points in
+    # between, both signs
+    pos = table[:127]
+    mids = (pos[:-1] + pos[1:]) / 2
+    rng = np.random.default_rng(5)
+    t = np.concatenate([pos, mids, mids * (1 + 1e-3), mids * (1 - 1e-3),
+                        rng.uniform(0, 460, 500), np.exp2(rng.uniform(-12, 9, 500))])
+    t = np.concatenate([t, -t])
+    got = np.asarray(dist(t), np.float64)
+    want = brute_midpoint_distance(t, table)
+    assert np.array_equal(got, want)
+
+
+def check_e4m3_output_close(close, table: np.ndarray):
+    """``close(codes, y_ref, out_scale) -> {"ok": bool, ...}`` for E4M3
+    product outputs: codes within one step of c_ref = E4M3(y_ref / os)
+    (0x00 and 0x80 equal), equal to c_ref wherever t = y_ref / os is
+    farther than 1e-3 (|t| + rms(t)) from a rounding midpoint, and
+    ||dec(code) - clip(t)||_F <= 2^-4 ||clip(t)||_F."""
+    enc = {float(table[c]): c for c in range(127)}
+    os_ = np.float32(0.5)
+    # t = 1.0 for every element (the code 0x38); far from both midpoints
+    # (0.03125 away; the window is 2e-3)
+    t = np.full((4, 8), 1.0)
+    y_ref = t * np.float64(os_)
+    c = np.full(t.shape, enc[1.0], np.uint8)
+    assert close(c, y_ref, os_)["ok"]
+    # one step off there is rejected (a window grown 1000-fold would let it
+    # through), and so is every other wrong code far from a midpoint
+    for wrong in (enc[1.125], enc[0.9375]):
+        cc = c.copy()
+        cc[1, 2] = wrong
+        assert not close(cc, y_ref, os_)["ok"], hex(wrong)
+    # t just below the midpoint 1.0625 (inside the window): c_ref = 0x38
+    # (1.0); the neighbour 0x39 (1.125) is accepted, 0x3A (1.25) is not
+    t = np.full((4, 8), 1.0)
+    t[2, 5] = 1.0625 - 1e-4
+    y_ref = t * np.float64(os_)
+    cc = np.full(t.shape, enc[1.0], np.uint8)
+    assert close(cc, y_ref, os_)["ok"]
+    cc[2, 5] = enc[1.125]
+    assert close(cc, y_ref, os_)["ok"]
+    cc[2, 5] = enc[1.25]
+    assert not close(cc, y_ref, os_)["ok"]
+    # a wrong sign is many steps away
+    cc[2, 5] = 0x80 | enc[1.0]
+    assert not close(cc, y_ref, os_)["ok"]
+    # signed zero: tiny negative references round to 0x80; 0x00 is the same
+    # value and is accepted, in both directions.  (Beside 16 values of 0.5,
+    # which keep the Frobenius error small and the window at ~5e-4.)
+    half = np.full(16, enc[0.5], np.uint8)
+    t = np.concatenate([np.full(16, 0.5), [-1e-5, 1e-5, -1e-6]]).reshape(1, -1)
+    y_ref = t * np.float64(os_)
+    zeros = lambda a, b, c: np.concatenate([half, np.array([a, b, c], np.uint8)]).reshape(1, -1)
+    assert close(zeros(0x80, 0x00, 0x80), y_ref, os_)["ok"]
+    assert close(zeros(0x00, 0x80, 0x00), y_ref, os_)["ok"]
+    # ... but the smallest subnormal is a step away from zero and t = -1e-5
+    # is far from the first midpoint (2^-10): rejected
+    assert not close(zeros(0x81, 0x00, 0x80), y_ref, os_)["ok"]
+    # saturated references: |t| >= 448 must give 0x7E / 0xFE; 0x7D (416) is
+    # a step below, far from any midpoint of the clipped value
+    t = np.array([[1000.0, -600.0, 448.0, 1.0]])
+    y_ref = t * np.float64(os_)
+    good = np.array([[0x7E, 0xFE, 0x7E, enc[1.0]]], np.uint8)
+    res = close(good, y_ref, os_)
+    assert res["ok"] and res["rel_fro"] == 0.0, res
+    bad = good.copy()
+    bad[0, 0] = 0x7D
+    assert not close(bad, y_ref, os_)["ok"]
+    # the Frobenius bound: references on the midpoint between the two
+    # smallest subnormals (1.5 * 2^-9) carry a relative error of 1/3 even
+    # with the nearest codes, which the bound rejects
+    t = np.full((2, 3), 1.5 * 2.0 ** -9)
+    y_ref = t * np.float64(os_)
+    res = close(np.full(t.shape, 0x02, np.uint8), y_ref, os_)
+    assert not res["ok"] and res["max_step"] == 0, res
+    # NaN codes are rejected
+    t = np.full((2, 2), 1.0)
+    cc = np.full(t.shape, enc[1.0], np.uint8)
+    cc[0, 1] = 0x7F
+    assert not close(cc, t * np.float64(os_), os_)["ok"]
+    # the output scale divides: the same codes against y_ref = 4 os t pass
+    # only with the codes of 4 t
+    t = np.full((3, 3), 1.0)
+    y_ref = 4.0 * t * np.float64(os_)
+    assert close(np.full(t.shape, enc[4.0], np.uint8), y_ref, os_)["ok"]
+    assert not close(np.full(t.shape, enc[1.0], np.uint8), y_ref, os_)["ok"]

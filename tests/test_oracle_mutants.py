@@ -198,3 +198,114 @@ def test_w8a16_mutants_rejected(table, mistake):
 
 def test_w8a16_copy_without_mistake_passes(table):
     pins.check_w8a16(_w8a16_mutant(None, table), table)
+
+
+# ---------------------------------------------------------------------------
+# parity criteria: copies of the acceptance functions with planted mistakes
+
+def _gemm_close_mutant(mistake):
+    def close(y, y_ref):
+        y = np.asarray(y, np.float64)
+        y_ref = np.asarray(y_ref, np.float64)
+        if y.size == 0:
+            return {"ok": True}
+        ref_for_bound = y if mistake == "bound_from_y" else y_ref
+        rms = float(np.sqrt(np.mean(ref_for_bound ** 2)))
+        err = np.abs(y - y_ref)
+        term = 0.0 if mistake == "no_rms_term" else rms
+        bound = 1e-2 * (np.abs(ref_for_bound) + term)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            ratio = np.where(bound > 0, err / bound, np.where(err > 0, np.inf, 0.0))
+        max_ratio = float(np.max(ratio))
+        denom = {"fro_over_y_norm": np.linalg.norm(y), "abs_fro": 1.0}.get(
+            mistake, np.linalg.norm(y_ref))
+        num = np.linalg.norm(y - y_ref)
+        if mistake == "squared_fro":
+            num, denom = num ** 2, denom ** 2
+        rel = float(num / denom) if denom > 0 else float(np.linalg.norm(y))
+        finite = bool(np.all(np.isfinite(y)))
+        fro_ok = True if mistake == "elementwise_only" else rel <= 5e-3
+        return {"ok": finite and max_ratio <= 1.0 and fro_ok}
+    return close
+
+
+@pytest.mark.parametrize("mistake", ["bound_from_y", "no_rms_term", "fro_over_y_norm",
+                                     "abs_fro", "squared_fro", "elementwise_only"])
+def test_gemm_close_mutants_rejected(mistake):
+    with pytest.raises(AssertionError):
+        pins.check_gemm_close(_gemm_close_mutant(mistake))
+
+
+def test_gemm_close_copy_without_mistake_passes():
+    pins.check_gemm_close(_gemm_close_mutant(None))
+
+
+def _midpoint_mutant(mistake, table):
+    def dist(t):
+        pos = table[:127]
+        mids = (pos[:-1] + pos[1:]) / 2
+        a = np.asarray(t, np.float64)
+        a = a if mistake == "no_abs" else np.abs(a)
+        if mistake != "no_clip":
+            a = np.minimum(a, 448.0)
+        i = np.clip(np.searchsorted(mids, a), 1, len(mids) - 1)
+        if mistake == "off_by_one":
+            i = np.clip(i + 1, 1, len(mids) - 1)
+        if mistake == "one_side":
+            return np.abs(a - mids[i])
+        return np.minimum(np.abs(a - mids[i - 1]), np.abs(a - mids[i]))
+    return dist
+
+
+@pytest.mark.parametrize("mistake", ["no_abs", "no_clip", "off_by_one", "one_side"])
+def test_midpoint_mutants_rejected(table, mistake):
+    with pytest.raises(AssertionError):
+        pins.check_midpoint_distance(_midpoint_mutant(mistake, table), table)
+
+
+def test_midpoint_copy_without_mistake_passes(table):
+    pins.check_midpoint_distance(_midpoint_mutant(None, table), table)
+
+
+def _e4m3_close_mutant(mistake, table):
+    def ordinal(c):
+        c = np.asarray(c, np.int64)
+        mag = c & 0x7F
+        if mistake == "signed_zero_distinct":
+            return np.where(c & 0x80, -mag - 1, mag)
+        return np.where(c & 0x80, -mag, mag)
+
+    def close(codes, y_ref, out_scale):
+        codes = np.asarray(codes, np.uint8)
+        y_ref = np.asarray(y_ref, np.float64)
+        os_ = np.float64(np.float32(out_scale))
+        t = y_ref if mistake == "scale_not_divided" else y_ref / os_
+        c_ref = oracle.e4m3_encode(t)
+        step = np.abs(ordinal(codes) - ordinal(c_ref))
+        rms = float(np.sqrt(np.mean(t ** 2)))
+        window = 1e-3 * (1000.0 if mistake == "window_x1000" else 1.0)
+        far = oracle._nearest_midpoint_distance(t) > window * (np.abs(t) + rms)
+        exact_bad = int(np.count_nonzero(far & (step != 0)))
+        if mistake == "no_exactness":
+            exact_bad = 0
+        tc = np.clip(t, -448.0, 448.0)
+        dec = table[codes]
+        nref = float(np.linalg.norm(tc))
+        rel = float(np.linalg.norm(dec - tc) / nref) if nref > 0 else float(np.linalg.norm(dec))
+        max_step = int(step.max()) if step.size else 0
+        allowed = 2 if mistake == "two_steps" else 1
+        fro_ok = True if mistake == "no_fro" else rel <= 2.0 ** -4
+        ok = max_step <= allowed and exact_bad == 0 and fro_ok and not np.any(np.isnan(dec))
+        return {"ok": ok, "max_step": max_step, "rel_fro": rel}
+    return close
+
+
+@pytest.mark.parametrize("mistake", ["signed_zero_distinct", "scale_not_divided",
+                                     "window_x1000", "no_exactness", "two_steps", "no_fro"])
+def test_e4m3_close_mutants_rejected(table, mistake):
+    with pytest.raises(AssertionError):
+        pins.check_e4m3_output_close(_e4m3_close_mutant(mistake, table), table)
+
+
+def test_e4m3_close_copy_without_mistake_passes(table):
+    pins.check_e4m3_output_close(_e4m3_close_mutant(None, table), table)
