@@ -24,6 +24,11 @@ What each function follows (page title, then the part of the page):
   * per-token activation scales (one per row of the activation codes): the
     RFC's Scope, which leaves scales finer than per-tensor for later; read
     as one scale per activation row.
+  * RMS normalization before the quantizer: "Condition to achieve linear
+    speedup?", where the activation quantization is fused into an
+    element-wise kernel such as RMSNorm; the pages do not define RMSNorm,
+    so the plain (Llama) definition is used, its output stored in the
+    activation's 16-bit format, then quantized as above.
 """
 from __future__ import annotations
 
@@ -85,6 +90,10 @@ def _load():
                                            P, ctypes.c_int, P]
         lib.fp8o_scaled_mm_rows_f64.argtypes = [P, P, I64, I64, I64, P, P, ctypes.c_int, P]
         lib.fp8o_w8a16_mm_f64.argtypes = [P, P, P, I64, I64, I64, P]
+        lib.fp8o_rmsnorm_f64.argtypes = [P, P, I64, I64, ctypes.c_double, P]
+        lib.fp8o_round_binary.argtypes = [ctypes.c_double, ctypes.c_int, ctypes.c_int]
+        lib.fp8o_round_binary.restype = ctypes.c_double
+        lib.fp8o_round_binary_array.argtypes = [P, I64, ctypes.c_int, ctypes.c_int, P]
         _lib = lib
         return lib
 
@@ -267,6 +276,57 @@ def e4m3_output_ref(y_ref, out_scale) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------
+# RMS normalization feeding the quantizer
+
+# (significand bits with the implicit one, minimum normal exponent)
+FORMATS = {"bf16": (8, -126), "fp16": (11, -14)}
+
+
+def _fmt(dtype) -> str:
+    name = str(dtype).replace("torch.", "")
+    return {"bfloat16": "bf16", "float16": "fp16", "bf16": "bf16", "fp16": "fp16"}[name]
+
+
+def rmsnorm_ref(x, gamma, eps) -> np.ndarray:
+    """h = x * gamma / sqrt(mean_k x^2 + eps) per row, in float64 (C loops)."""
+    xf = widen(x)
+    gf = widen(gamma).reshape(-1)
+    assert xf.ndim == 2 and gf.size == xf.shape[1]
+    h = np.empty(xf.shape, np.float64)
+    _load().fp8o_rmsnorm_f64(_ptr(xf), _ptr(np.ascontiguousarray(gf)), xf.shape[0], xf.shape[1],
+                             float(eps), _ptr(h))
+    return h
+
+
+def round_to(v, dtype) -> np.ndarray:
+    """Round float64 values to the nearest bf16 / fp16 value (ties to even,
+    gradual underflow), returned as float64."""
+    p, emin = FORMATS[_fmt(dtype)]
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, np.float64)
+    _load().fp8o_round_binary_array(_ptr(v), v.size, p, emin, _ptr(out))
+    return out
+
+
+def rmsnorm_quant(x, gamma, eps, mode="tensor", scale=None):
+    """The layer's normalization followed by quantization, as the unfused
+    layer computes it: h = RMSNorm(x) stored in x's 16-bit format, then
+    per-tensor (dynamic or static) or per-row quantization of h.  Returns
+    (codes, scale(s), h as float64 of the 16-bit values)."""
+    import torch
+    dt = x.dtype if isinstance(x, torch.Tensor) else x
+    h = round_to(rmsnorm_ref(x, gamma, eps), dt)
+    h32 = h.astype(np.float32)  # exact: every 16-bit value is a float32
+    if mode == "row":
+        q, s = quant_per_row(h32)
+    elif mode == "tensor":
+        q, s = quant_per_tensor(h32, scale)
+    else:
+        raise ValueError(mode)
+    return q, s, h
+
+
+# --------------------------------------------------------------------------
 # parity criteria (used by the tests, the smoke check and the benchmark)
 
 GEMM_ELEMENT_TOL = 1e-2   # |y - y_ref| <= 1e-2 (|y_ref| + rms(y_ref)) per element
@@ -294,6 +354,31 @@ def gemm_close(y, y_ref) -> dict:
     rel_fro = float(np.linalg.norm(y - y_ref) / nref) if nref > 0 else float(np.linalg.norm(y))
     ok = bool(np.all(np.isfinite(y))) and max_ratio <= 1.0 and rel_fro <= GEMM_FRO_TOL
     return {"ok": ok, "max_ratio": max_ratio, "rel_fro": rel_fro}
+
+
+NORM_MIDPOINT_WINDOW = 2.0 ** -16  # relative; see rounded_close
+
+
+def rounded_close(h, h_ref, dtype, window=NORM_MIDPOINT_WINDOW) -> dict:
+    """Tolerance of a 16-bit result h computed in float32 against the
+    float64 reference h_ref of the same operation: h must be the rounding
+    of h_ref to the format (ties to even), except where h_ref lies within
+    ``window * |h_ref|`` of a rounding midpoint, where either neighbour is
+    accepted.  The window covers the float32 evaluation's relative error
+    (below 2^-17 for a sum of at most 2^16 squares, a square root, a
+    reciprocal and two products)."""
+    p, emin = FORMATS[_fmt(dtype)]
+    h = np.asarray(h, np.float64)
+    h_ref = np.asarray(h_ref, np.float64)
+    assert h.shape == h_ref.shape
+    want = round_to(h_ref, dtype)
+    lo = round_to(h_ref * (1 - window), dtype)
+    hi = round_to(h_ref * (1 + window), dtype)
+    exact = h == want
+    either = (h == lo) | (h == hi)
+    ok_each = exact | either
+    bad = int(np.count_nonzero(~ok_each | ~np.isfinite(h)))
+    return {"ok": bad == 0, "bad": bad, "differing": int(np.count_nonzero(~exact))}
 
 
 def _signed_ordinal(codes):

@@ -228,3 +228,47 @@ void fp8o_w8a16_mm_f64(const float *x, const uint8_t *qw, const float *sw,
         }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* RMS normalization feeding the quantizer.  "Condition to achieve linear
+ * speedup?" (the QQQ issue) names fusing the activation quantization into
+ * an element-wise kernel such as RMSNorm; the pages do not define RMSNorm,
+ * so this is its plain reading (the Llama layer norm):
+ *   h[m,k] = x[m,k] * gamma[k] / sqrt( (1/K) sum_j x[m,j]^2 + eps )
+ * in double precision.  The layer stores h in the activation's 16-bit
+ * format before quantizing it: fp8o_round_binary rounds a double to the
+ * nearest value of a binary format with `p` significand bits (including the
+ * implicit one) and minimum normal exponent `emin`, ties to even, with
+ * gradual underflow (bfloat16: p = 8, emin = -126; fp16: p = 11,
+ * emin = -14).  Values beyond the format's range are not produced by the
+ * inputs used here.                                                        */
+
+void fp8o_rmsnorm_f64(const float *x, const float *gamma, int64_t M, int64_t K,
+                      double eps, double *h)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; ++k)
+            ss += (double)x[m * K + k] * (double)x[m * K + k];
+        double rms = sqrt(ss / (double)K + eps);
+        for (int64_t k = 0; k < K; ++k)
+            h[m * K + k] = (double)x[m * K + k] * (double)gamma[k] / rms;
+    }
+}
+
+double fp8o_round_binary(double v, int p, int emin)
+{
+    if (v == 0.0 || v != v)
+        return v;
+    int e = ilogb(v);
+    if (e < emin)
+        e = emin;
+    double ulp = ldexp(1.0, e - (p - 1));
+    return rint(v / ulp) * ulp; /* v / ulp is exact; rint rounds ties to even */
+}
+
+void fp8o_round_binary_array(const double *v, int64_t n, int p, int emin, double *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = fp8o_round_binary(v[i], p, emin);
+}

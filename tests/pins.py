@@ -532,3 +532,104 @@ def check_e4m3_output_close(close, table: np.ndarray):
     y_ref = 4.0 * t * np.float64(os_)
     assert close(np.full(t.shape, enc[4.0], np.uint8), y_ref, os_)["ok"]
     assert not close(np.full(t.shape, enc[1.0], np.uint8), y_ref, os_)["ok"]
+
+
+# ---------------------------------------------------------------------------
+# RMS normalization: ``norm(x_torch16 [M, K], gamma_torch16 [K], eps) ->
+# h float64 [M, K]`` (h = x gamma / sqrt(mean_k x^2 + eps) per row)
+
+def check_rmsnorm(norm):
+    # constant rows, eps = 0: every h is +-gamma exactly (c^2 and sqrt(c^2)
+    # are exact); rows of different constants are independent
+    K = 48
+    g = torch.Generator().manual_seed(1)
+    gamma = (torch.rand(K, generator=g) + 0.5).to(torch.bfloat16)
+    x = torch.tensor([[1.5] * K, [-0.375] * K, [96.0] * K], dtype=torch.bfloat16)
+    h = norm(x, gamma, 0.0)
+    gf = gamma.double().numpy()
+    want = np.stack([gf, -gf, gf])
+    assert np.array_equal(h, want), (h - want)
+    # eps = 3 c^2: the root is 2|c|, h = +-gamma / 2 exactly
+    h = norm(x[:1], gamma, 3 * 1.5 ** 2)
+    assert np.array_equal(h, gf[None, :] / 2)
+    # a single nonzero element a in a row of K = 64: mean = a^2 / 64, the
+    # root is |a| / 8, so h = 8 sign(a) gamma there and 0 elsewhere
+    K = 64
+    gamma = torch.linspace(0.5, 2.0, K).to(torch.bfloat16)
+    x = torch.zeros((2, K), dtype=torch.bfloat16)
+    x[0, 5] = 3.0
+    x[1, 60] = -0.25
+    h = norm(x, gamma, 0.0)
+    gf = gamma.double().numpy()
+    want = np.zeros((2, K))
+    want[0, 5] = 8 * gf[5]
+    want[1, 60] = -8 * gf[60]
+    assert np.array_equal(h, want)
+    # random rows, gamma = 1, eps = 0: mean(h^2) = 1 per row; powers of two
+    # of x leave h unchanged; permuting the columns of x and gamma together
+    # permutes h
+    x = torch.randn((5, 96), generator=g).to(torch.bfloat16)
+    ones = torch.ones(96, dtype=torch.bfloat16)
+    h = norm(x, ones, 0.0)
+    assert np.allclose((h ** 2).mean(axis=1), 1.0, rtol=1e-13)
+    assert np.array_equal(norm((x.float() * 8).to(torch.bfloat16), ones, 0.0), h)
+    gamma = (torch.rand(96, generator=g) + 0.5).to(torch.bfloat16)
+    perm = torch.randperm(96, generator=g)
+    h = norm(x, gamma, 1e-5)
+    hp = norm(x[:, perm], gamma[perm], 1e-5)
+    assert np.array_equal(hp, h[:, perm.numpy()])
+    # eps matters: against the closed form sqrt(ms / (ms + eps)) of mean(h^2)
+    h = norm(x, ones, 0.5)
+    ms = (x.double().numpy() ** 2).mean(axis=1)
+    assert np.allclose((h ** 2).mean(axis=1), ms / (ms + 0.5), rtol=1e-13)
+
+
+# ``rnd(v float64 array, dtype) -> float64 array`` of the nearest bf16 /
+# fp16 values, ties to even
+def check_round_to(rnd):
+    for dt in (torch.bfloat16, torch.float16):
+        one = 1.0
+        p = 8 if dt == torch.bfloat16 else 11
+        u = 2.0 ** -(p - 1)  # spacing at 1
+        # ties: 1 + u/2 -> 1 (even), 1 + 3u/2 -> 1 + 2u (even)
+        got = rnd(np.array([one + u / 2, one + 3 * u / 2, -(one + u / 2), one + u / 2 + 2.0 ** -40]), dt)
+        assert np.array_equal(got, [1.0, 1.0 + 2 * u, -1.0, 1.0 + u]), (dt, got)
+        # the library cast of float32 values (one rounding) agrees, including
+        # subnormals of the format and values right at midpoints
+        rng = np.random.default_rng(3)
+        v = (rng.standard_normal(100_000) * np.exp2(rng.uniform(-30, 14, 100_000))).astype(np.float32)
+        lib = torch.from_numpy(v).to(dt).double().numpy()
+        assert np.array_equal(rnd(v.astype(np.float64), dt), lib), dt
+        vals = torch.from_numpy(all_16bit_values(dt)).double().numpy()
+        vals = np.unique(vals[np.isfinite(vals) & (vals > 0)])
+        mids = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)  # exact in float32
+        lib = torch.from_numpy(mids).to(dt).double().numpy()
+        assert np.array_equal(rnd(mids.astype(np.float64), dt), lib), dt
+
+
+# ``close(h, h_ref, dtype) -> {"ok": ...}``: h must be the rounding of h_ref,
+# or either neighbour within a relative window 2^-16 of a midpoint
+def check_rounded_close(close):
+    dt = torch.bfloat16
+    u = 2.0 ** -7
+    h_ref = np.array([1.0 + 0.3 * u, 2.0 + 2 * 0.7 * u, -3.0])
+    want = np.array([1.0, 2.0 + 2 * u, -3.0])
+    assert close(want, h_ref, dt)["ok"]
+    # one unit off far from a midpoint: rejected, in either direction
+    for i, d in ((0, u), (1, -2 * u), (2, 2 * u)):
+        h = want.copy()
+        h[i] += d
+        assert not close(h, h_ref, dt)["ok"], (i, d)
+    # h_ref just above the midpoint 1 + u/2 (inside the window): 1 + u is the
+    # rounding, 1 is accepted too, 1 + 2u is not
+    h_ref = np.array([1.0 + u / 2 + 2.0 ** -22])
+    assert close(np.array([1.0 + u]), h_ref, dt)["ok"]
+    assert close(np.array([1.0]), h_ref, dt)["ok"]
+    assert not close(np.array([1.0 + 2 * u]), h_ref, dt)["ok"]
+    # ... but 2^-14 above it is outside the window: only 1 + u
+    h_ref = np.array([1.0 + u / 2 + 2.0 ** -14])
+    assert close(np.array([1.0 + u]), h_ref, dt)["ok"]
+    assert not close(np.array([1.0]), h_ref, dt)["ok"]
+    # non-finite results are rejected
+    assert not close(np.array([np.nan]), np.array([1.0]), dt)["ok"]
+    assert not close(np.array([np.inf]), np.array([1.0]), dt)["ok"]

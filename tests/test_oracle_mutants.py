@@ -309,3 +309,95 @@ def test_e4m3_close_mutants_rejected(table, mistake):
 
 def test_e4m3_close_copy_without_mistake_passes(table):
     pins.check_e4m3_output_close(_e4m3_close_mutant(None, table), table)
+
+
+# ---------------------------------------------------------------------------
+# RMS normalization, 16-bit rounding and its acceptance function
+
+def _norm_mutant(mistake):
+    def norm(x, gamma, eps):
+        X = oracle.widen(x).astype(np.float64)
+        G = oracle.widen(gamma).astype(np.float64).reshape(-1)
+        axis = 0 if mistake == "over_columns" else 1
+        ss = (X ** 2).sum(axis=axis, keepdims=True)
+        ms = ss if mistake == "sum_not_mean" else ss / X.shape[axis]
+        if mistake == "eps_outside_sqrt":
+            rms = np.sqrt(ms) + eps
+        elif mistake == "no_sqrt":
+            rms = ms + eps
+        else:
+            rms = np.sqrt(ms + eps)
+        if mistake == "gamma_reversed":
+            G = G[::-1]
+        if mistake == "gamma_divides":
+            return X / G / rms
+        return X * G / rms
+    return norm
+
+
+@pytest.mark.parametrize("mistake", ["over_columns", "sum_not_mean", "eps_outside_sqrt",
+                                     "no_sqrt", "gamma_reversed", "gamma_divides"])
+def test_rmsnorm_mutants_rejected(mistake):
+    with pytest.raises(AssertionError):
+        pins.check_rmsnorm(_norm_mutant(mistake))
+
+
+def test_rmsnorm_copy_without_mistake_passes():
+    pins.check_rmsnorm(_norm_mutant(None))
+
+
+def _round_mutant(mistake):
+    def rnd(v, dtype):
+        p, emin = oracle.FORMATS[oracle._fmt(dtype)]
+        v = np.asarray(v, np.float64)
+        out = np.empty_like(v)
+        for i, x in enumerate(v.reshape(-1)):
+            if x == 0:
+                out.reshape(-1)[i] = x
+                continue
+            e = max(int(np.floor(np.log2(abs(x)))), emin)
+            if mistake == "flush_subnormals" and abs(x) < 2.0 ** emin:
+                out.reshape(-1)[i] = 0.0
+                continue
+            ulp = 2.0 ** (e - (p - 1))
+            t = x / ulp
+            if mistake == "ties_away":
+                r = np.sign(t) * np.floor(abs(t) + 0.5)
+            elif mistake == "truncate":
+                r = np.trunc(t)
+            else:
+                r = np.rint(t)
+            out.reshape(-1)[i] = r * ulp
+        return out
+    return rnd
+
+
+@pytest.mark.parametrize("mistake", ["ties_away", "truncate", "flush_subnormals"])
+def test_round_to_mutants_rejected(mistake):
+    with pytest.raises(AssertionError):
+        pins.check_round_to(_round_mutant(mistake))
+
+
+def _rounded_close_mutant(mistake):
+    def close(h, h_ref, dtype):
+        h = np.asarray(h, np.float64)
+        h_ref = np.asarray(h_ref, np.float64)
+        window = {"window_x1000": 2.0 ** -16 * 1000, "no_window": 0.0}.get(mistake, 2.0 ** -16)
+        want = oracle.round_to(h_ref, dtype)
+        lo = oracle.round_to(h_ref * (1 - window), dtype)
+        hi = oracle.round_to(h_ref * (1 + window), dtype)
+        ok = (h == want) | (h == lo) | (h == hi)
+        if mistake == "nan_ok":
+            ok |= np.isnan(h)
+        return {"ok": bool(np.all(ok))}
+    return close
+
+
+@pytest.mark.parametrize("mistake", ["window_x1000", "no_window", "nan_ok"])
+def test_rounded_close_mutants_rejected(mistake):
+    with pytest.raises(AssertionError):
+        pins.check_rounded_close(_rounded_close_mutant(mistake))
+
+
+def test_rounded_close_copy_without_mistake_passes():
+    pins.check_rounded_close(_rounded_close_mutant(None))
