@@ -17,10 +17,11 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfp8linear.so")
 
-ABI_VERSION = 2  # the library version this binding is written for
+ABI_VERSION = 3  # the library version this binding is written for
 F16, BF16, E4M3, F32 = 0, 1, 2, 3
 WEIGHTS_STABLE = 1
 WEIGHTS_PACKED = 2
+A_PER_TOKEN = 4
 OK, EINVAL, ESHAPE, EALIGN, ECUDA, ETIMEOUT, EUNSUPPORTED = range(7)
 
 _DTYPE_CODE = {torch.float16: F16, torch.bfloat16: BF16, torch.float32: F32,
@@ -63,6 +64,8 @@ def load():
         lib.fp8l_strerror.argtypes = [I]
         lib.fp8l_read_status.restype = I
         lib.fp8l_read_status.argtypes = [P, P]
+        lib.fp8l_debug_waits.restype = I
+        lib.fp8l_debug_waits.argtypes = [ctypes.c_longlong, ctypes.c_uint]
         lib.fp8_quant_per_tensor.restype = I
         lib.fp8_quant_per_tensor.argtypes = [P, I, I64, I64, P, P, I, P, P]
         lib.fp8_quant_per_row.restype = I
@@ -75,6 +78,8 @@ def load():
         lib.fp8_packed_weight_bytes.argtypes = [I64, I64]
         lib.fp8_pack_w8a16_weights.restype = I
         lib.fp8_pack_w8a16_weights.argtypes = [P, I64, I64, P, P]
+        lib.fp8_rmsnorm_quant.restype = I
+        lib.fp8_rmsnorm_quant.argtypes = [P, I, P, ctypes.c_float, I64, I64, P, P, I, P, P, P]
         _lib = lib
         return lib
 
@@ -124,6 +129,18 @@ def fp8l_read_status(ws: torch.Tensor) -> int:
         return int(load().fp8l_read_status(ws.data_ptr(), _stream(ws.device)))
 
 
+STALL_MMA = 1
+STALL_GRID = 2
+
+
+def fp8l_debug_waits(wait_cycles: int = 0, stall_mask: int = 0) -> None:
+    """Testing hook: shorten the device-side wait limit (cycles; 0 = default)
+    and make the given waits target a barrier that nothing completes
+    (STALL_MMA, STALL_GRID).  Process-wide; fp8l_debug_waits() restores the
+    defaults."""
+    _check(load().fp8l_debug_waits(int(wait_cycles), int(stall_mask)), "fp8l_debug_waits")
+
+
 def fp8_quant_per_tensor(x: torch.Tensor, q: torch.Tensor | None = None,
                          scale: torch.Tensor | None = None, dynamic: bool = True,
                          ws: torch.Tensor | None = None):
@@ -149,6 +166,46 @@ def fp8_quant_per_tensor(x: torch.Tensor, q: torch.Tensor | None = None,
     return q, scale
 
 
+NQ_MODES = {"dynamic": 0, "static": 1, "per_token": 2, "norm_only": 3}
+
+
+def fp8_rmsnorm_quant(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-5,
+                      mode: str = "dynamic", q: torch.Tensor | None = None,
+                      scale: torch.Tensor | None = None, h: torch.Tensor | None = None,
+                      want_h: bool = False, ws: torch.Tensor | None = None):
+    """RMSNorm of x [M, K] (fp16/bf16) with gamma [K], fused with its E4M3
+    quantization.  mode: "dynamic" (per-tensor scale written), "static"
+    (scale given), "per_token" (M scales written) or "norm_only" (h only).
+    Returns (q uint8 or None, scale or None, h or None); h is written when
+    given, when want_h, or in norm_only mode."""
+    _need_cuda(x, gamma, q, scale, h, ws)
+    if x.dim() != 2 or gamma.shape != (x.shape[1],) or gamma.dtype != x.dtype:
+        raise ValueError("expected x [M, K] and gamma [K] of the same dtype")
+    M, K = x.shape
+    m = NQ_MODES[mode]
+    if (want_h or mode == "norm_only") and h is None:
+        h = torch.empty_like(x)
+    if mode != "norm_only":
+        if q is None:
+            q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+        if scale is None:
+            if mode == "static":
+                raise ValueError("static mode needs a scale tensor")
+            scale = torch.empty(M if mode == "per_token" else 1, dtype=torch.float32,
+                                device=x.device)
+    if mode == "dynamic" and ws is None:
+        ws = workspace(x.device)
+    with torch.cuda.device(x.device):
+        st = load().fp8_rmsnorm_quant(
+            x.data_ptr(), _DTYPE_CODE[x.dtype], gamma.data_ptr(), float(eps), M, K,
+            _codes(q).data_ptr() if q is not None else None,
+            scale.data_ptr() if scale is not None else None, m,
+            h.data_ptr() if h is not None else None,
+            ws.data_ptr() if ws is not None else None, _stream(x.device))
+    _check(st, "fp8_rmsnorm_quant")
+    return q, scale, h
+
+
 def fp8_quant_per_row(x: torch.Tensor, q: torch.Tensor | None = None,
                       row_scale: torch.Tensor | None = None):
     """One dynamic scale per row of a 2-D tensor.  Returns (q uint8, scales float32[rows])."""
@@ -171,11 +228,14 @@ def fp8_quant_per_row(x: torch.Tensor, q: torch.Tensor | None = None,
 def fp8_scaled_mm(a: torch.Tensor, w: torch.Tensor, a_scale: torch.Tensor,
                   w_scale: torch.Tensor, out_dtype=torch.bfloat16,
                   out_scale: torch.Tensor | None = None, y: torch.Tensor | None = None,
-                  ws: torch.Tensor | None = None, stable_weights: bool = False) -> torch.Tensor:
-    """W8A8 product of E4M3 a [M, K] and w [N, K] with per-tensor a_scale and a
-    per-tensor ([1]) or per-channel ([N]) w_scale.  out_dtype bf16 / fp16, or
-    uint8 (E4M3 codes, needs out_scale).  stable_weights sets
-    FP8L_WEIGHTS_STABLE (no work in flight on the stream writes w or w_scale)."""
+                  ws: torch.Tensor | None = None, stable_weights: bool = False,
+                  per_token: bool | None = None) -> torch.Tensor:
+    """W8A8 product of E4M3 a [M, K] and w [N, K] with a per-tensor ([1]) or
+    per-token ([M]) a_scale and a per-tensor ([1]) or per-channel ([N])
+    w_scale.  out_dtype bf16 / fp16, or uint8 (E4M3 codes, needs out_scale).
+    stable_weights sets FP8L_WEIGHTS_STABLE (no work in flight on the stream
+    writes w or w_scale); per_token (default: a_scale has M > 1 entries) sets
+    FP8L_A_PER_TOKEN."""
     _need_cuda(a, w, a_scale, w_scale, out_scale, y, ws)
     a, w = _codes(a), _codes(w)
     M, K = a.shape
@@ -192,12 +252,16 @@ def fp8_scaled_mm(a: torch.Tensor, w: torch.Tensor, a_scale: torch.Tensor,
     per_channel = 1 if w_scale.numel() == N and N != 1 else 0
     if w_scale.numel() not in (1, N):
         raise ValueError("w_scale must have 1 or N entries")
+    if per_token is None:
+        per_token = a_scale.numel() == M and M > 1
+    if a_scale.numel() != (M if per_token else 1):
+        raise ValueError("a_scale must have 1 entry, or M with per_token")
+    flags = (WEIGHTS_STABLE if stable_weights else 0) | (A_PER_TOKEN if per_token else 0)
     with torch.cuda.device(a.device):
         st = load().fp8_scaled_mm(
             a.data_ptr(), w.data_ptr(), M, N, K, a_scale.data_ptr(), w_scale.data_ptr(),
             per_channel, out_scale.data_ptr() if out_scale is not None else None,
-            _codes(y).data_ptr(), code, ws.data_ptr(), WEIGHTS_STABLE if stable_weights else 0,
-            _stream(a.device))
+            _codes(y).data_ptr(), code, ws.data_ptr(), flags, _stream(a.device))
     _check(st, "fp8_scaled_mm")
     return y
 

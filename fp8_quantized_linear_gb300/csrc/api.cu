@@ -9,6 +9,16 @@
 namespace fp8l {
 
 namespace {
+std::atomic<long long> g_wait_cycles{0};
+std::atomic<unsigned> g_stall{0};
+}  // namespace
+
+WaitConfig wait_config() {
+    const long long c = g_wait_cycles.load(std::memory_order_relaxed);
+    return WaitConfig{c > 0 ? c : kDefaultWaitCycles, g_stall.load(std::memory_order_relaxed)};
+}
+
+namespace {
 constexpr int kMaxDevices = 64;
 // 0 = unknown, 1 = supported, 2 = unsupported; SM count beside it
 std::atomic<int> g_dev_state[kMaxDevices];
@@ -66,15 +76,49 @@ int make_kmajor_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, 
     return r == CUDA_SUCCESS ? FP8L_OK : FP8L_ECUDA;
 }
 
+int current_context_id(unsigned long long *id) {
+    static std::atomic<PFN_cuCtxGetCurrent_v4000> get_cur{nullptr};
+    static std::atomic<PFN_cuCtxGetId_v12000> get_id{nullptr};
+    PFN_cuCtxGetCurrent_v4000 fc = get_cur.load(std::memory_order_acquire);
+    PFN_cuCtxGetId_v12000 fi = get_id.load(std::memory_order_acquire);
+    if (fc == nullptr || fi == nullptr) {
+        void *p = nullptr, *q = nullptr;
+        cudaDriverEntryPointQueryResult r1, r2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &r1) !=
+                cudaSuccess ||
+            r1 != cudaDriverEntryPointSuccess ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &q, 12000, cudaEnableDefault, &r2) !=
+                cudaSuccess ||
+            r2 != cudaDriverEntryPointSuccess)
+            return FP8L_ECUDA;
+        fc = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        fi = reinterpret_cast<PFN_cuCtxGetId_v12000>(q);
+        get_cur.store(fc, std::memory_order_release);
+        get_id.store(fi, std::memory_order_release);
+    }
+    CUcontext ctx = nullptr;
+    if (fc(&ctx) != CUDA_SUCCESS) return FP8L_ECUDA;
+    if (ctx == nullptr) {
+        *id = 0;
+        return FP8L_OK;
+    }
+    return fi(ctx, id) == CUDA_SUCCESS ? FP8L_OK : FP8L_ECUDA;
+}
+
 namespace {
-// waits for `s`, reads the workspace status word at `dev`, clears it if set
-int read_and_clear(unsigned *dev, cudaStream_t s) {
+// Waits for `s` and reads the status word at the start of workspace `ws`.
+// A set word is cleared; after a time-out the whole barrier area [0, 32) is
+// zeroed too (ticket, call counter, arrival counts, maximum words), since the
+// call that gave up may have left them part-way through a grid barrier.
+int read_and_clear(void *ws, cudaStream_t s) {
     unsigned host = 0;
+    unsigned *dev = status_word(ws);
     if (cudaMemcpyAsync(&host, dev, sizeof(unsigned), cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return FP8L_ECUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return FP8L_ECUDA;
     if (host != 0u) {
-        if (cudaMemsetAsync(dev, 0, sizeof(unsigned), s) != cudaSuccess) return FP8L_ECUDA;
+        const size_t bytes = (host & kStatusTimeout) ? kBarrierAreaBytes : sizeof(unsigned);
+        if (cudaMemsetAsync(ws, 0, bytes, s) != cudaSuccess) return FP8L_ECUDA;
         if (cudaStreamSynchronize(s) != cudaSuccess) return FP8L_ECUDA;
     }
     return (host & kStatusTimeout) ? FP8L_ETIMEOUT : FP8L_OK;
@@ -102,10 +146,18 @@ const char *fp8l_strerror(int status) {
     }
 }
 
+int fp8l_debug_waits(long long wait_cycles, unsigned stall_mask) {
+    if (wait_cycles < 0 || (stall_mask & ~(fp8l::kStallMma | fp8l::kStallGrid)) != 0u)
+        return FP8L_EINVAL;
+    fp8l::g_wait_cycles.store(wait_cycles, std::memory_order_relaxed);
+    fp8l::g_stall.store(stall_mask, std::memory_order_relaxed);
+    return FP8L_OK;
+}
+
 int fp8l_read_status(void *workspace, void *stream) {
     if (workspace == nullptr) return FP8L_EINVAL;
     if (!fp8l::aligned16(workspace)) return FP8L_EALIGN;
-    return fp8l::read_and_clear(fp8l::status_word(workspace), fp8l::as_stream(stream));
+    return fp8l::read_and_clear(workspace, fp8l::as_stream(stream));
 }
 
 }  // extern "C"

@@ -20,11 +20,26 @@ namespace fp8l {
 //                            call starts; that call clears the other pair)
 //   [256, 256 + 4*kMaxParts) float per-block partial maxima (two-launch quantizer)
 constexpr size_t kStatusOffset = 0;
+constexpr size_t kBarrierAreaBytes = 32;  // [0, 32): status and barrier words
 constexpr size_t kPartialsOffset = 256;
 constexpr int kMaxPartials = 2048;
 constexpr size_t kWorkspaceBytes = kPartialsOffset + sizeof(float) * kMaxPartials;
 
 constexpr unsigned kStatusTimeout = 1u;  // a bounded device-side wait gave up
+
+// Limits of the bounded device-side waits, in SM clock cycles.  The default
+// is ~2 s at 2 GHz (a healthy wait takes microseconds).  fp8l_debug_waits may
+// shorten the limit of the main waits and make one wait target a barrier
+// that nothing completes (testing the time-out path); waits that drain
+// copies in flight before a block exits always keep the default.
+constexpr long long kDefaultWaitCycles = 4LL << 30;
+constexpr unsigned kStallMma = 1u;   // product: the MMA role's first wait never completes
+constexpr unsigned kStallGrid = 2u;  // quantizer: the grid barrier waits for one block too many
+struct WaitConfig {
+    long long cycles;  // limit of the main waits
+    unsigned stall;    // kStall* bits
+};
+WaitConfig wait_config();
 
 // Largest magnitude of OCP E4M3.
 constexpr float kE4M3Max = 448.0f;
@@ -66,6 +81,11 @@ inline float *partials(void *workspace) {
 // answer and the SM count per device ordinal.
 int check_device(int *sm_count_out);
 
+// Unique id of the CUDA context current on this thread (0 when none is):
+// the driver's cuCtxGetId, which never repeats within a process, so a
+// context created after cudaDeviceReset gets a new id.
+int current_context_id(unsigned long long *id);
+
 // 2-D TMA map over a row-major [rows, K] byte matrix: box box_k x box_rows,
 // 128-byte swizzle, zero fill outside the matrix.
 int make_kmajor_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_k,
@@ -78,9 +98,9 @@ inline int launch_status() {
 
 // Launchers shared between translation units.
 int launch_skinny_e4m3(const uint8_t *a, const uint8_t *w, int M, int N, int K,
-                       const float *a_scale, const float *w_scale, int w_per_channel,
-                       const float *out_scale, void *y, int out_dtype, bool stable_weights,
-                       cudaStream_t stream);
+                       const float *a_scale, int a_per_token, const float *w_scale,
+                       int w_per_channel, const float *out_scale, void *y, int out_dtype,
+                       bool stable_weights, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // device helpers

@@ -5,7 +5,8 @@
 // their scales; "Marlin fp8": per-output-channel weight scales; "RFC: FP8
 // Quantization Schema in vLLM": output_scale for an E4M3 result.)
 //
-//   y[m, n] = cast( sum_k dec(a[m,k]) dec(w[n,k]) * a_scale * w_scale(n) )
+//   y[m, n] = cast( sum_k dec(a[m,k]) dec(w[n,k]) * a_scale(m) * w_scale(n) )
+//   (a_scale(m) = a_scale[m] with per-token activation scales, else a_scale[0])
 //
 // Structure (one persistent CTA per SM, 192 threads):
 //   warp 0      TMA producer: 128x128 A tile and 256x128 W tile per k-block
@@ -52,19 +53,19 @@ constexpr int kEpiWarps = 4;
 constexpr int kNumBarriers = 2 * STAGES + 2 + 2 + 1;
 constexpr size_t kSmemBytes = 1024 + size_t(STAGES) * kStageBytes + kNumBarriers * 8 + 16;
 
-// ~2 s at 2 GHz: a healthy wait in this kernel is microseconds
-constexpr long long kWaitCycles = 4LL << 30;
-
 struct GemmParams {
     int M, N, K;
     int num_m_blocks, num_n_blocks, num_k_blocks;
     const float *a_scale;
     const float *w_scale;
     int w_per_channel;
+    int a_per_token;  // a_scale has M entries
     const float *out_scale;
     void *y;
     int out_dtype;
     unsigned *status;
+    long long wait_cycles;  // limit of the main waits (kDefaultWaitCycles unless a test shortened it)
+    unsigned stall;         // kStallMma: testing the time-out path
     int split;  // > 1: a cluster of `split` CTAs shares one tile and splits its k-blocks
 };
 
@@ -96,17 +97,17 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 }
 
 // Bounded wait for the phase of parity `parity`.  Gives up when another
-// role raised the abort flag, or after kWaitCycles (then raises it and
+// role raised the abort flag, or after `limit` cycles (then raises it and
 // records the time-out).
 __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                       unsigned *status) {
+                                       unsigned *status, long long limit) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0u) {
             if (*abort_flag) return false;
-            if (clock64() - t0 > kWaitCycles) {
+            if (clock64() - t0 > limit) {
                 *abort_flag = 1;
                 atomicOr(status, kStatusTimeout);
                 return false;
@@ -119,7 +120,7 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
 __device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, unsigned *status) {
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > kDefaultWaitCycles) {
             atomicOr(status, kStatusTimeout);
             return false;
         }
@@ -229,13 +230,13 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
         __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
 }
 
-// Scales and stores 32 accumulator columns [n0, n0+32) of row m.
+// Scales and stores 32 accumulator columns [n0, n0+32) of row m; sa is the
+// row's activation scale and sa_sw = sa * w_scale[0].
 __device__ __forceinline__ void store_row_chunk(const GemmParams &p, const uint32_t (&r)[32],
-                                                int m, int n0, float sa_sw) {
+                                                int m, int n0, float sa, float sa_sw) {
     const bool full32 = n0 + 32 <= p.N;  // N % 16 == 0: else exactly 16 columns remain
     float v[32];
     if (p.w_per_channel) {
-        const float sa = __ldg(p.a_scale);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             const float sw = (j < 16 || full32) ? __ldg(p.w_scale + n0 + j) : 0.0f;
@@ -286,7 +287,7 @@ __device__ void split_reduce_store(const GemmParams &p, int tile, int rank, uint
     const int r0 = rank * rows_per;
     const int r1 = r0 + rows_per < BM ? r0 + rows_per : BM;
     const int items = (r1 - r0) * (BN / 4);
-    const float sa = __ldg(p.a_scale);
+    const float sa0 = __ldg(p.a_scale);
     const float sw0 = __ldg(p.w_scale);
     for (int i = threadIdx.x; i < items; i += blockDim.x) {
         const int row = r0 + i / (BN / 4);
@@ -304,6 +305,7 @@ __device__ void split_reduce_store(const GemmParams &p, int tile, int rank, uint
             acc.w += v.w;
         }
         float v[4] = {acc.x, acc.y, acc.z, acc.w};
+        const float sa = p.a_per_token ? __ldg(p.a_scale + m) : sa0;
 #pragma unroll
         for (int j = 0; j < 4; ++j)
             v[j] *= sa * (p.w_per_channel ? __ldg(p.w_scale + n + j) : sw0);
@@ -395,7 +397,7 @@ gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
                 const int mb = tile % p.num_m_blocks;
                 const int nb = tile / p.num_m_blocks;
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.wait_cycles)) {
                         ok = false;
                         break;
                     }
@@ -423,12 +425,15 @@ gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
+            // testing the time-out path: wait for a barrier that nothing
+            // completes before this role's own commit below
+            if (p.stall & kStallMma) ok = mbar_wait(done_bar, 0, abort_flag, p.status, p.wait_cycles);
             for (int tile = tile_begin; ok && tile < num_tiles; tile += tile_step) {
-                if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) break;
+                if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status, p.wait_cycles)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
-                    if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) {
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status, p.wait_cycles)) {
                         ok = false;
                         break;
                     }
@@ -458,14 +463,14 @@ gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
     } else {
         const int quarter = warp & 3;  // TMEM lanes this warp may read: 32*quarter ..
         const int row = quarter * 32 + lane;
-        float sa_sw = 0.0f;
-        if (!p.w_per_channel) sa_sw = __ldg(p.a_scale) * __ldg(p.w_scale);
+        const float sa0 = __ldg(p.a_scale);
+        const float sw0 = __ldg(p.w_scale);
         int acc = 0;
         uint32_t acc_phase = 0;
         if (split) {
             // fp32 partial tile into the (now idle) stage ring: part[row][col],
             // row pitch kPartPitch floats
-            if (mbar_wait(tfull_bar(0), 0, abort_flag, p.status)) {
+            if (mbar_wait(tfull_bar(0), 0, abort_flag, p.status, p.wait_cycles)) {
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
                 const uint32_t prow = sbase + static_cast<uint32_t>(row * kPartPitch * 4);
@@ -484,9 +489,11 @@ gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
         for (int tile = split ? num_tiles : tile_begin; tile < num_tiles; tile += tile_step) {
             const int mb = tile % p.num_m_blocks;
             const int nb = tile / p.num_m_blocks;
-            if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status)) break;
+            if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status, p.wait_cycles)) break;
             tc_fence_after();
             const int m = mb * BM + row;
+            const float sa = p.a_per_token ? (m < p.M ? __ldg(p.a_scale + m) : 0.0f) : sa0;
+            const float sa_sw = sa * sw0;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
@@ -494,7 +501,7 @@ gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
                 uint32_t r[32];
                 tmem_ld32(taddr + static_cast<uint32_t>(c * 32), r);
                 const int n0 = nb * BN + c * 32;
-                if (m < p.M && n0 < p.N) store_row_chunk(p, r, m, n0, sa_sw);
+                if (m < p.M && n0 < p.N) store_row_chunk(p, r, m, n0, sa, sa_sw);
             }
             tc_fence_before();
             __syncwarp();
@@ -544,7 +551,8 @@ int ensure_smem_attr() {
 }
 
 int launch_tcgen05(const uint8_t *a, const uint8_t *w, int M, int N, int K, const float *a_scale,
-                   const float *w_scale, int w_per_channel, const float *out_scale, void *y,
+                   int a_per_token, const float *w_scale, int w_per_channel,
+                   const float *out_scale, void *y,
                    int out_dtype, unsigned *status, int sms, cudaStream_t stream) {
     CUtensorMap ma, mb;
     if (make_map(&ma, a, M, K, BM) != FP8L_OK) return FP8L_ECUDA;
@@ -560,10 +568,14 @@ int launch_tcgen05(const uint8_t *a, const uint8_t *w, int M, int N, int K, cons
     p.a_scale = a_scale;
     p.w_scale = w_scale;
     p.w_per_channel = w_per_channel;
+    p.a_per_token = a_per_token;
     p.out_scale = out_scale;
     p.y = y;
     p.out_dtype = out_dtype;
     p.status = status;
+    const WaitConfig wc = wait_config();
+    p.wait_cycles = wc.cycles;
+    p.stall = wc.stall;
     const int64_t tiles = int64_t(p.num_m_blocks) * p.num_n_blocks;
     // Few tiles (small M): a cluster of `split` CTAs per tile splits K so
     // that most SMs stream weights; otherwise one persistent CTA per SM.
@@ -601,7 +613,7 @@ extern "C" int fp8_scaled_mm(const uint8_t *a, const uint8_t *w, int64_t M, int6
     using namespace fp8l;
     if (out_dtype != FP8L_F16 && out_dtype != FP8L_BF16 && out_dtype != FP8L_E4M3)
         return FP8L_EINVAL;
-    if ((flags & ~FP8L_WEIGHTS_STABLE) != 0u) return FP8L_EINVAL;
+    if ((flags & ~(FP8L_WEIGHTS_STABLE | FP8L_A_PER_TOKEN)) != 0u) return FP8L_EINVAL;
     if (a_scale == nullptr || w_scale == nullptr || workspace == nullptr || w == nullptr)
         return FP8L_EINVAL;
     if (out_dtype == FP8L_E4M3 && out_scale == nullptr) return FP8L_EINVAL;
@@ -620,11 +632,12 @@ extern "C" int fp8_scaled_mm(const uint8_t *a, const uint8_t *w, int64_t M, int6
     if (M == 0) return FP8L_OK;
     cudaStream_t s = as_stream(stream);
     const int pc = w_per_channel ? 1 : 0;
+    const int pt = (flags & FP8L_A_PER_TOKEN) != 0u ? 1 : 0;
     if (M <= 16)
         return launch_skinny_e4m3(a, w, static_cast<int>(M), static_cast<int>(N),
-                                  static_cast<int>(K), a_scale, w_scale, pc, out_scale, y,
+                                  static_cast<int>(K), a_scale, pt, w_scale, pc, out_scale, y,
                                   out_dtype, (flags & FP8L_WEIGHTS_STABLE) != 0u, s);
     return launch_tcgen05(a, w, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                          a_scale, w_scale, pc, out_scale, y, out_dtype, status_word(workspace),
-                          sms, s);
+                          a_scale, pt, w_scale, pc, out_scale, y, out_dtype,
+                          status_word(workspace), sms, s);
 }

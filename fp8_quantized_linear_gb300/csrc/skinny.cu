@@ -53,7 +53,8 @@ struct SkinnyArgs {
     const uint8_t *w;  // [N, K] E4M3
     const void *x;     // [M, K] f16 / bf16 / E4M3
     int M, N, K;
-    const float *a_scale;    // E4M3 activations only
+    const float *a_scale;    // E4M3 activations only: [1], or [M] per token
+    int a_per_token;
     const float *w_scale;    // [1] or [N]
     int w_per_channel;
     const float *out_scale;  // E4M3 output only
@@ -269,7 +270,7 @@ skinny_kernel(const SkinnyArgs args) {
         for (int wi = 0; wi < WARPS; ++wi) sum += red[wi][nt][r][lane_src];
         const int n = n0 + ch;
         float sc = args.w_per_channel ? __ldg(args.w_scale + n) : __ldg(args.w_scale);
-        if constexpr (XK == kXE4M3) sc *= ld_act_f32(args.a_scale);
+        if constexpr (XK == kXE4M3) sc *= ld_act_f32(args.a_scale + (args.a_per_token ? m : 0));
         const float v = sum * sc;
         const size_t yi = static_cast<size_t>(m) * args.N + n;
         if (args.out_dtype == FP8L_F16) {
@@ -340,10 +341,11 @@ __global__ void pack_weights_kernel(const uint8_t *__restrict__ w, int N, int K,
 }  // namespace
 
 int launch_skinny_e4m3(const uint8_t *a, const uint8_t *w, int M, int N, int K,
-                       const float *a_scale, const float *w_scale, int w_per_channel,
-                       const float *out_scale, void *y, int out_dtype, bool stable_weights,
-                       cudaStream_t stream) {
-    SkinnyArgs args{w, a, M, N, K, a_scale, w_scale, w_per_channel, out_scale, y, out_dtype};
+                       const float *a_scale, int a_per_token, const float *w_scale,
+                       int w_per_channel, const float *out_scale, void *y, int out_dtype,
+                       bool stable_weights, cudaStream_t stream) {
+    SkinnyArgs args{w,       a,           M,         N, K, a_scale, a_per_token,
+                    w_scale, w_per_channel, out_scale, y, out_dtype};
     return launch<kXE4M3>(args, stable_weights, stream);
 }
 
@@ -393,7 +395,7 @@ extern "C" int fp8_w8a16_mm(const void *x, int x_dtype, const uint8_t *w, const 
     int st = check_device(nullptr);
     if (st != FP8L_OK) return st;
     SkinnyArgs args{w, x, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                    nullptr, w_scale, 1, nullptr, y, x_dtype};
+                    nullptr, 0, w_scale, 1, nullptr, y, x_dtype};
     const bool stable = (flags & FP8L_WEIGHTS_STABLE) != 0u;
     const cudaStream_t s = as_stream(stream);
     if ((flags & FP8L_WEIGHTS_PACKED) != 0u)

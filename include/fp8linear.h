@@ -47,9 +47,11 @@ extern "C" {
 #endif
 
 /* ABI version (fp8l_abi_version): 1, the first release; 2 adds
- * fp8_pack_w8a16_weights, fp8_packed_weight_bytes and FP8L_WEIGHTS_PACKED.
- * The change is additive: a caller written for version 1 runs unchanged. */
-#define FP8L_ABI_VERSION 2
+ * fp8_pack_w8a16_weights, fp8_packed_weight_bytes and FP8L_WEIGHTS_PACKED;
+ * 3 adds fp8l_debug_waits, the per-token activation scales
+ * (FP8L_A_PER_TOKEN) and fp8_rmsnorm_quant.  Each change is additive: a caller written for an
+ * earlier version runs unchanged. */
+#define FP8L_ABI_VERSION 3
 
 /* Only the entry points below are exported from the shared library. */
 #if defined(__GNUC__)
@@ -86,6 +88,11 @@ enum fp8l_status {
  * packed layout written by fp8_pack_w8a16_weights, not as [N, K] rows. */
 #define FP8L_WEIGHTS_PACKED 2u
 
+/* FP8L_A_PER_TOKEN (fp8_scaled_mm only): a_scale holds M values, one per
+ * row of `a` (per-token activation scales, as fp8_quant_per_row computes
+ * them for activations), instead of one. */
+#define FP8L_A_PER_TOKEN 4u
+
 /* Element types. */
 enum fp8l_dtype {
     FP8L_F16 = 0,   /* IEEE binary16                                         */
@@ -101,9 +108,9 @@ enum fp8l_dtype {
  * a device status word and the dynamic quantizer's grid-barrier words (a call
  * counter, two arrival counts and two maximum words used by alternate calls,
  * and per-block partial maxima); the library keeps nothing else in it between
- * calls.  After a call reports FP8L_ETIMEOUT (fp8l_read_status) the barrier
- * words may be left mid-call: fill the workspace with zeros again before the
- * next call. */
+ * calls.  A call whose device-side wait gave up may leave the barrier words
+ * mid-call; fp8l_read_status, when it reports FP8L_ETIMEOUT, zeroes them
+ * (bytes [0, 32)) before it returns, so the workspace is ready again. */
 FP8L_API size_t fp8l_workspace_bytes(void);
 
 /* Per-tensor quantization of a [rows, cols] activation or weight tensor
@@ -148,19 +155,25 @@ FP8L_API int fp8_quant_per_row(const void *x, int x_dtype, int64_t rows, int64_t
  * through output_scale: "RFC: FP8 Quantization Schema in vLLM").
  *
  *   acc[m,n] = sum_k dec(a[m,k]) * dec(w[n,k])      (fp32 accumulation)
- *   v[m,n]   = acc[m,n] * a_scale[0] * ws(n)        ws(n) = w_scale[n] when
- *                                                   w_per_channel, else w_scale[0]
+ *   v[m,n]   = acc[m,n] * as(m) * ws(n)             ws(n) = w_scale[n] when
+ *                                                   w_per_channel, else w_scale[0];
+ *                                                   as(m) = a_scale[m] with
+ *                                                   FP8L_A_PER_TOKEN, else a_scale[0]
  *   out_dtype FP8L_BF16 / FP8L_F16: y[m,n] = v[m,n] rounded to nearest
  *   out_dtype FP8L_E4M3:            y[m,n] = E4M3(v[m,n] / out_scale[0])
  *
  * a: [M, K] E4M3 codes; w: [N, K] E4M3 codes; y: [M, N] of out_dtype.
- * a_scale: 1 float; w_scale: 1 or N floats; out_scale: 1 float, required
+ * a_scale: 1 float (M floats with FP8L_A_PER_TOKEN: finer-than-per-tensor
+ * scales, which "RFC: FP8 Quantization Schema in vLLM", Scope, leaves for
+ * later; read here as one scale per token); w_scale: 1 or N floats;
+ * out_scale: 1 float, required
  * when out_dtype is FP8L_E4M3 and ignored otherwise.
  * M >= 0 (M == 0 launches nothing); N and K are positive multiples of 16
  * (the FP8 GEMM shape rule), N, K <= 2^20, M <= 2^31 - 1.
  * M <= 16 runs a weight-streaming kernel; larger M runs the tcgen05 tensor
  * core kernel.  workspace: fp8l_workspace_bytes() bytes (status word).
- * flags: 0 or FP8L_WEIGHTS_STABLE (other bits are FP8L_EINVAL). */
+ * flags: any of FP8L_WEIGHTS_STABLE and FP8L_A_PER_TOKEN (other bits are
+ * FP8L_EINVAL). */
 FP8L_API int fp8_scaled_mm(const uint8_t *a, const uint8_t *w, int64_t M, int64_t N,
                   int64_t K, const float *a_scale, const float *w_scale,
                   int w_per_channel, const float *out_scale, void *y,
@@ -208,6 +221,38 @@ FP8L_API size_t fp8_packed_weight_bytes(int64_t N, int64_t K);
 FP8L_API int fp8_pack_w8a16_weights(const uint8_t *w, int64_t N, int64_t K,
                                     uint8_t *w_packed, void *stream);
 
+/* Modes of fp8_rmsnorm_quant. */
+#define FP8L_NQ_DYNAMIC 0   /* per-tensor scale amax|h| / 448, written to *scale    */
+#define FP8L_NQ_STATIC 1    /* per-tensor scale read from *scale (input_scale)     */
+#define FP8L_NQ_PER_TOKEN 2 /* scale[m] = amax_k |h[m,k]| / 448, M scales written   */
+#define FP8L_NQ_NORM_ONLY 3 /* h only, no codes: the unfused layer's norm step     */
+
+/* RMS normalization with the activation quantization fused into it
+ * ("Condition to achieve linear speedup?": the quantization of the
+ * activations is fused into the element-wise kernel before the product,
+ * such as RMSNorm, instead of a separate pass; the pages do not define
+ * RMSNorm, so this is the plain Llama definition).  Per row m:
+ *
+ *   r[m]   = 1 / sqrt( (1/K) sum_k x[m,k]^2 + eps )   (float32, IEEE ops)
+ *   h[m,k] = RN16( (x[m,k] * r[m]) * gamma[k] )      (x's 16-bit format)
+ *   codes  = the E4M3 quantization of h, exactly as fp8_quant_per_tensor
+ *            (FP8L_NQ_DYNAMIC / FP8L_NQ_STATIC) or fp8_quant_per_row
+ *            (FP8L_NQ_PER_TOKEN) quantize the 16-bit tensor h.
+ *
+ * x: [M, K] of x_dtype (FP8L_F16 or FP8L_BF16); gamma: [K] of x_dtype;
+ * eps >= 0 and finite.  q: [M, K] uint8 codes (unused in FP8L_NQ_NORM_ONLY).
+ * scale: 1 float (written in FP8L_NQ_DYNAMIC, read in FP8L_NQ_STATIC) or M
+ * floats (FP8L_NQ_PER_TOKEN); unused in FP8L_NQ_NORM_ONLY.  h: NULL, or
+ * [M, K] of x_dtype receiving the normalized activations (required in
+ * FP8L_NQ_NORM_ONLY); the codes are the same whether or not h is written.
+ * workspace: fp8l_workspace_bytes() bytes, required in FP8L_NQ_DYNAMIC
+ * (grid barrier words and status word), optional otherwise (status word).
+ * K is a positive multiple of 16 and at most 32768; 0 <= M <= 2^31 - 1
+ * (M == 0 writes only the dynamic scale, 1.0f).  Deterministic. */
+FP8L_API int fp8_rmsnorm_quant(const void *x, int x_dtype, const void *gamma, float eps,
+                               int64_t M, int64_t K, uint8_t *q, float *scale, int mode,
+                               void *h, void *workspace, void *stream);
+
 /* Dynamic per-tensor quantization that allocates nothing and takes no
  * workspace.  The pages have no counterpart to this entry point.
  *
@@ -232,17 +277,47 @@ FP8L_API int fp8_pack_w8a16_weights(const uint8_t *w, int64_t N, int64_t K,
  * entries it reads.
  *
  * Set-up: the first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current) and keeps it; make that
- * first call before any stream capture begins.  The entry point calls no
- * cudaMalloc, cudaFree or other allocating routine. */
+ * (cudaGetSymbolAddress, with that device current) and keeps it together with
+ * the id of the CUDA context it was taken in; a call made while another
+ * context is current on that device (a context created after
+ * cudaDeviceReset, or the caller's own) looks it up again for that context.
+ * Make the first call in each context before any stream capture begins.
+ * The entry point calls no cudaMalloc, cudaFree or other allocating
+ * routine. */
 FP8L_API int fp8_quant_per_tensor_noalloc(const void *x, int x_dtype, int64_t rows,
                                           int64_t cols, uint8_t *q, float *scale,
                                           void *stream);
 
 /* Waits for `stream`, then reads and clears the workspace's status word.
  * Returns FP8L_OK, FP8L_ETIMEOUT if a device-side wait of an earlier call
- * gave up (that call's outputs are then undefined), or FP8L_ECUDA. */
+ * gave up (that call's outputs are then undefined; the workspace's barrier
+ * words are zeroed as well, so the next call starts clean), or FP8L_ECUDA. */
 FP8L_API int fp8l_read_status(void *workspace, void *stream);
+
+/* Testing hook for the bounded device-side waits (this library's failure
+ * detection; the pages have no counterpart).  Every device-side wait of the
+ * tcgen05 product and of the dynamic quantizer gives up after a limit,
+ * records FP8L_ETIMEOUT in the workspace status word, lets the block's
+ * copies in flight land, frees what the block holds and returns, so the
+ * CUDA context stays usable.  This call lets a test drive that path without
+ * faulting or hanging a GPU.  For every later launch, on every device:
+ *   wait_cycles > 0    limit, in SM clock cycles, of the main waits (the
+ *                      product's stage and accumulator waits, the
+ *                      quantizer's stage waits and grid barrier); 0 restores
+ *                      the default of 2^32 cycles (about 2 s).  Waits that
+ *                      drain copies in flight before a block exits always
+ *                      keep the default.
+ *   FP8L_STALL_MMA     the product's MMA role first waits on a barrier that
+ *                      nothing completes;
+ *   FP8L_STALL_GRID    the dynamic quantizer's grid barrier waits for one
+ *                      block more than the grid has.
+ * A stalled call's outputs are undefined; fp8l_read_status reports
+ * FP8L_ETIMEOUT and resets the workspace.  The setting is process-wide and
+ * meant for tests only.  Returns FP8L_EINVAL for a negative limit or an
+ * unknown bit. */
+#define FP8L_STALL_MMA 1u
+#define FP8L_STALL_GRID 2u
+FP8L_API int fp8l_debug_waits(long long wait_cycles, unsigned stall_mask);
 
 /* Static, human-readable name of a status code. */
 FP8L_API const char *fp8l_strerror(int status);

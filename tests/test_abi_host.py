@@ -54,7 +54,7 @@ def test_only_c_abi_symbols_exported(lib):
 
 def test_constants(lib):
     import fp8_quantized_linear_gb300 as fl
-    assert lib.fp8l_abi_version() == fl._binding.ABI_VERSION == 2
+    assert lib.fp8l_abi_version() == fl._binding.ABI_VERSION == 3
     assert fl.fp8l_workspace_bytes() >= 4096 and fl.fp8l_workspace_bytes() % 16 == 0
     for code in range(7):
         assert fl.strerror(code)
@@ -140,6 +140,16 @@ def test_quant_argument_errors(lib):
     assert g(A16, b.BF16, 4, 24, A16, A16, None) == b.ESHAPE
     assert g(A16, 9, 4, 32, A16, A16, None) == b.EINVAL
     assert g(A16, b.BF16, 4, 32, None, A16, None) == b.EINVAL
+
+
+def test_debug_waits_argument_errors(lib):
+    import fp8_quantized_linear_gb300._binding as b
+    lib.fp8l_debug_waits.restype = ctypes.c_int
+    lib.fp8l_debug_waits.argtypes = [ctypes.c_longlong, ctypes.c_uint]
+    assert lib.fp8l_debug_waits(-1, 0) == b.EINVAL
+    assert lib.fp8l_debug_waits(0, 4) == b.EINVAL
+    assert lib.fp8l_debug_waits(1 << 20, b.STALL_MMA | b.STALL_GRID) == b.OK
+    assert lib.fp8l_debug_waits(0, 0) == b.OK  # back to the defaults
 
 
 def test_read_status_argument_errors(lib):
