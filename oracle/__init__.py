@@ -24,6 +24,9 @@ What each function follows (page title, then the part of the page):
   * per-token activation scales (one per row of the activation codes): the
     RFC's Scope, which leaves scales finer than per-tensor for later; read
     as one scale per activation row.
+  * grouped products for mixture-of-experts layers: "RFC: FP8 Quantization
+    Schema in vLLM", the gate_proj question (FP8 products need shapes
+    divisible by 16; the experts' products are FP8).
   * RMS normalization before the quantizer: "Condition to achieve linear
     speedup?", where the activation quantization is fused into an
     element-wise kernel such as RMSNorm; the pages do not define RMSNorm,
@@ -91,6 +94,8 @@ def _load():
         lib.fp8o_scaled_mm_rows_f64.argtypes = [P, P, I64, I64, I64, P, P, ctypes.c_int, P]
         lib.fp8o_w8a16_mm_f64.argtypes = [P, P, P, I64, I64, I64, P]
         lib.fp8o_rmsnorm_f64.argtypes = [P, P, I64, I64, ctypes.c_double, P]
+        lib.fp8o_grouped_mm_f64.argtypes = [P, P, P, I64, I64, I64, I64, P, ctypes.c_int, P,
+                                            ctypes.c_int, P]
         lib.fp8o_round_binary.argtypes = [ctypes.c_double, ctypes.c_int, ctypes.c_int]
         lib.fp8o_round_binary.restype = ctypes.c_double
         lib.fp8o_round_binary_array.argtypes = [P, I64, ctypes.c_int, ctypes.c_int, P]
@@ -243,6 +248,45 @@ def scaled_mm_ref(qa, qw, sa, sw) -> np.ndarray:
     sa = _act_scales(sa, A.shape[0]).astype(np.float64)
     acc = A @ W.T
     return acc * (sa.reshape(-1, 1) * sw.reshape(1, -1))
+
+
+def grouped_mm_bruteforce(qa, qw, offsets, sa, sw) -> np.ndarray:
+    """Grouped product by loops (C): rows offsets[e] .. offsets[e+1]-1 of qa
+    use expert e's weights qw[e] [N, K] and scales sw[e] (one, or N).
+    Rows outside every group are left 0."""
+    qa = np.ascontiguousarray(qa, dtype=np.uint8)
+    qw = np.ascontiguousarray(qw, dtype=np.uint8)
+    offs = np.ascontiguousarray(offsets, dtype=np.int32)
+    M, K = qa.shape
+    E, N, K2 = qw.shape
+    assert K == K2 and offs.size == E + 1
+    sw = np.ascontiguousarray(np.asarray(sw, np.float32).reshape(E, -1))
+    assert sw.shape[1] in (1, N)
+    sa = _act_scales(sa, M)
+    y = np.zeros((M, N), dtype=np.float64)
+    _load().fp8o_grouped_mm_f64(_ptr(qa), _ptr(qw), _ptr(offs), E, M, N, K, _ptr(sa),
+                                int(sa.size == M and M != 1), _ptr(sw),
+                                int(sw.shape[1] == N and N != 1), _ptr(y))
+    return y
+
+
+def grouped_mm_ref(qa, qw, offsets, sa, sw) -> np.ndarray:
+    """``grouped_mm_bruteforce`` through one float64 matrix product per
+    expert (library primitive)."""
+    qa = np.asarray(qa, dtype=np.uint8)
+    E, N, _ = np.asarray(qw).shape
+    M = qa.shape[0]
+    sw = np.asarray(sw, np.float32).reshape(E, -1)
+    sa = _act_scales(sa, M).astype(np.float64)
+    y = np.zeros((M, N), np.float64)
+    for e in range(E):
+        lo, hi = int(offsets[e]), min(int(offsets[e + 1]), M)
+        if hi <= lo:
+            continue
+        rows_sa = sa[lo:hi] if sa.size == M and M != 1 else sa[:1]
+        y[lo:hi] = scaled_mm_ref(qa[lo:hi], qw[e], rows_sa if rows_sa.size > 1 else rows_sa[0],
+                                 sw[e] if sw.shape[1] == N else sw[e, :1])
+    return y
 
 
 def w8a16_bruteforce(x, qw, sw) -> np.ndarray:

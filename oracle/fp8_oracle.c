@@ -272,3 +272,33 @@ void fp8o_round_binary_array(const double *v, int64_t n, int p, int emin, double
     for (int64_t i = 0; i < n; ++i)
         out[i] = fp8o_round_binary(v[i], p, emin);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Grouped W8A8 product for mixture-of-experts layers.  "RFC: FP8
+ * Quantization Schema in vLLM", the gate_proj question: FP8 GEMMs need
+ * shapes divisible by 16, which is why an 8-expert gate stays in 16-bit;
+ * the expert products themselves are FP8.  Tokens routed to expert e are
+ * the rows offs[e] .. offs[e+1]-1 of qa; expert e has its own weights
+ * qw[e] ([N, K]) and scales (one per expert, or N per expert):
+ *   y[m,n] = (sa(m) * sw_e(n)) * sum_k dec(qa[m,k]) * dec(qw[e][n,k])
+ * for offs[e] <= m < offs[e+1].  sa has 1 or M entries.                    */
+void fp8o_grouped_mm_f64(const uint8_t *qa, const uint8_t *qw, const int32_t *offs,
+                         int64_t E, int64_t M, int64_t N, int64_t K,
+                         const float *sa, int sa_per_row, const float *sw, int per_channel,
+                         double *y)
+{
+    const double *val = value_table();
+    for (int64_t e = 0; e < E; ++e) {
+        const uint8_t *we = qw + e * N * K;
+        for (int64_t m = offs[e]; m < offs[e + 1] && m < M; ++m) {
+            for (int64_t n = 0; n < N; ++n) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < K; ++k)
+                    acc += val[qa[m * K + k]] * val[we[n * K + k]];
+                double ws = per_channel ? (double)sw[e * N + n] : (double)sw[e];
+                double as = sa_per_row ? (double)sa[m] : (double)sa[0];
+                y[m * N + n] = (as * ws) * acc;
+            }
+        }
+    }
+}

@@ -633,3 +633,69 @@ def check_rounded_close(close):
     # non-finite results are rejected
     assert not close(np.array([np.nan]), np.array([1.0]), dt)["ok"]
     assert not close(np.array([np.inf]), np.array([1.0]), dt)["ok"]
+
+
+# ---------------------------------------------------------------------------
+# Grouped W8A8 product (mixture of experts):
+# ``gmm(qa [M, K], qw [E, N, K], offsets [E+1], sa (1 or M), sw (E or E x N))
+# -> y float64 [M, N]``; rows outside every group are 0
+
+def check_grouped_mm(gmm, table: np.ndarray):
+    one = _code_of(table, 1.0)
+    # all-ones operands: y[m, n] = K sa sw_e(n) for m in group e; groups of
+    # different sizes, an empty group, rows after the last group
+    E, N, K, M = 4, 32, 48, 23
+    offs = np.array([0, 5, 5, 16, 20], np.int32)  # expert 1 empty; rows 20..22 unrouted
+    qa = np.full((M, K), one, np.uint8)
+    qw = np.full((E, N, K), one, np.uint8)
+    sw = np.array([[2.0 ** (e - 2) * 2.0 ** (n % 5 - 2) for n in range(N)] for e in range(E)],
+                  np.float32)
+    y = gmm(qa, qw, offs, np.float32(0.5), sw)
+    assert y.shape == (M, N)
+    want = np.zeros((M, N))
+    for e in range(E):
+        want[offs[e]:offs[e + 1]] = K * 0.5 * sw[e][None, :]
+    assert np.array_equal(y, want), np.argwhere(y != want)[:5]
+    # one scale per expert
+    sw1 = np.array([[3.0], [5.0], [0.25], [7.0]], np.float32)
+    y = gmm(qa, qw, offs, np.float32(0.5), sw1)
+    want = np.zeros((M, N))
+    for e in range(E):
+        want[offs[e]:offs[e + 1]] = K * 0.5 * sw1[e, 0]
+    assert np.array_equal(y, want)
+    # a different permutation per expert: y[m, n] = sa sw_e[n] dec(qa[m, pi_e(n)])
+    K = N = 16
+    E, M = 3, 12
+    offs = np.array([0, 4, 9, 12], np.int32)
+    rng = np.random.default_rng(13)
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    qa = rng.choice(finite, size=(M, K)).astype(np.uint8)
+    pis = [[(a * n + b) % K for n in range(N)] for a, b in ((5, 3), (7, 1), (3, 10))]
+    qw = np.zeros((E, N, K), np.uint8)
+    for e in range(E):
+        for n in range(N):
+            qw[e, n, pis[e][n]] = one
+    sw = np.array([[2.0 ** ((n + e) % 5 - 2) for n in range(N)] for e in range(E)], np.float32)
+    sa = np.array([2.0 ** -(m % 3) for m in range(M)], np.float32)  # per token
+    y = gmm(qa, qw, offs, sa, sw)
+    want = np.zeros((M, N))
+    for e in range(E):
+        for m in range(offs[e], offs[e + 1]):
+            for n in range(N):
+                want[m, n] = float(sa[m]) * float(sw[e, n]) * table[qa[m, pis[e][n]]]
+    assert np.array_equal(y, want)
+    # exact integer arithmetic against Python integers
+    vals = [-2.0, -1.0, -0.5, 0.0, 0.5, 1.0, 2.0]
+    codes = np.array([_code_of(table, v) for v in vals], np.uint8)
+    E, M, N, K = 3, 10, 5, 40
+    offs = np.array([0, 2, 7, 10], np.int32)
+    ia = rng.integers(0, len(vals), size=(M, K))
+    iw = rng.integers(0, len(vals), size=(E, N, K))
+    sw = np.array([[0.5], [2.0], [0.125]], np.float32)
+    y = gmm(codes[ia], codes[iw], offs, np.float32(0.75), sw)
+    twice = [int(2 * v) for v in vals]
+    for e in range(E):
+        for m in range(offs[e], offs[e + 1]):
+            for n in range(N):
+                acc4 = sum(twice[ia[m, k]] * twice[iw[e, n, k]] for k in range(K))
+                assert y[m, n] == 0.75 * float(sw[e, 0]) * acc4 / 4.0, (e, m, n)

@@ -401,3 +401,42 @@ def test_rounded_close_mutants_rejected(mistake):
 
 def test_rounded_close_copy_without_mistake_passes():
     pins.check_rounded_close(_rounded_close_mutant(None))
+
+
+# ---------------------------------------------------------------------------
+# grouped product
+
+def _grouped_mutant(mistake, table):
+    def gmm(qa, qw, offs, sa, sw):
+        A = table[np.asarray(qa)]
+        W = table[np.asarray(qw)]
+        E, N, _ = W.shape
+        M = A.shape[0]
+        sw = np.asarray(sw, np.float64).reshape(E, -1)
+        sa = np.asarray(sa, np.float64).reshape(-1)
+        y = np.zeros((M, N))
+        for e in range(E):
+            lo, hi = int(offs[e]), int(offs[e + 1])
+            if mistake == "inclusive_end":
+                hi = min(hi + 1, M)
+            ew = (e + 1) % E if mistake == "next_expert" else e
+            es = 0 if mistake == "first_expert_scale" else e
+            for m in range(lo, hi):
+                scol = sw[es] if sw.shape[1] == N else np.full(N, sw[es, 0])
+                if mistake == "flat_channel_scale" and sw.shape[1] == N:
+                    scol = sw.reshape(-1)[:N]
+                s_m = sa[m] if sa.size == M and M != 1 else sa[0]
+                y[m] = (A[m] @ W[ew].T) * s_m * scol
+        return y
+    return gmm
+
+
+@pytest.mark.parametrize("mistake", ["inclusive_end", "next_expert", "first_expert_scale",
+                                     "flat_channel_scale"])
+def test_grouped_mutants_rejected(table, mistake):
+    with pytest.raises(AssertionError):
+        pins.check_grouped_mm(_grouped_mutant(mistake, table), table)
+
+
+def test_grouped_copy_without_mistake_passes(table):
+    pins.check_grouped_mm(_grouped_mutant(None, table), table)
