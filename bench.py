@@ -6,13 +6,22 @@
 
 One JSON line on stdout (rank 0).  A step is one pass of the layer over every
 shape of the workload:
-  * decode_w8a16 (default; the decode workload of the W8A16 path): the 12
-    fp16 x E4M3 products M in {1,4,16} x (N,K) in {(12288,4096),
-    (4096,4096), (22016,4096), (4096,11008)}; metric GB/s of algorithmic
-    bytes (2MK + NK + 2MN + 4N per product).
-  * prefill_w8a8_outliers / llama3_8b_w8a8_sweep / llama70b_static_fp8out:
-    activation quantization (dynamic or static) plus the W8A8 product of
-    every shape; metric TFLOP/s (2MNK), M <= 16 shapes also in GB/s.
+  * llama70b_static_fp8out (default, the largest workload): static
+    activation quantization plus the W8A8 product with per-channel weight
+    scales and E4M3 output (output_scale) of 16 shapes, M in {1,64,1024,4096}
+    x (N,K) in {(10240,8192),(8192,8192),(57344,8192),(8192,28672)}; metric
+    TFLOP/s (2MNK).
+  * decode_w8a16: the 12 fp16 x E4M3 products M in {1,4,16} x (N,K) in
+    {(12288,4096), (4096,4096), (22016,4096), (4096,11008)}; metric GB/s of
+    algorithmic bytes (2MK + NK + 2MN + 4N per product).
+  * prefill_w8a8_outliers / llama3_8b_w8a8_sweep / tiny_w8a8: dynamic
+    activation quantization plus the W8A8 product of every shape; TFLOP/s.
+With the default workload the line also carries one entry per other
+workload (same measurement, shorter), and every line carries per-shape
+figures: each product timed alone (a CUDA graph of the one call over
+rotating operand copies, replayed back to back, CUDA events outside the
+replays) against the roofline min(tensor peak, HBM bandwidth x arithmetic
+intensity), and, for M <= 16, against HBM bandwidth alone.
 Weights are quantized once before timing (untimed setup), as the layer does
 after loading; W8A16 weights are then packed into the kernel's fragment
 order (--w8a16-layout row-major keeps [N, K] rows).  Each shape owns its own weight buffer and, where a step's
@@ -23,8 +32,10 @@ The timed region replays a CUDA graph of one step K times (after W warm-up
 replays), bracketed by CUDA events on the launching stream; event-record
 nodes inside the graph time each kernel call, which gives the roofline
 figure of the dominant kernel.  The end-to-end figure runs the public API
-eagerly with pinned host buffers: host-to-device copies of the activations,
-the kernels, and device-to-host copies of the outputs, every step.
+with pinned host buffers: host-to-device copies of the activations, the
+kernels, and device-to-host copies of the outputs, every step.  Clocks,
+power and clock-event reasons are sampled through NVML (read-only queries)
+every 2 ms during the timed region.
 
 --impl reference times the CPU oracle (plain C loops, one thread) on a
 bounded sample of the same workload, in the same unit.
@@ -52,6 +63,9 @@ import torch  # noqa: E402
 import synthetic  # noqa: E402
 
 METRIC = "FP8 scaled-GEMM TFLOP/s (GB/s at M<=16) and % of GB300 roofline"
+HEADLINE = "llama70b_static_fp8out"
+ENTRY_WORKLOADS = ("decode_w8a16", "prefill_w8a8_outliers", "llama3_8b_w8a8_sweep", "tiny_w8a8")
+HBM_TARGET = 0.70  # fraction of HBM bandwidth the M <= 16 shapes aim for
 L2_BYTES = 126 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -66,10 +80,12 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=3000)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="decode_w8a16", choices=sorted(synthetic.WORKLOADS))
+    p.add_argument("--workload", default=HEADLINE, choices=sorted(synthetic.WORKLOADS))
     p.add_argument("--headline-only", action="store_true",
                    help="skip the other workloads' summary entries")
     p.add_argument("--extra-steps", type=int, default=20)
+    p.add_argument("--only-shape", type=int, default=None,
+                   help="profiling: run only this shape (index in the workload's list)")
     p.add_argument("--w8a16-layout", choices=["packed", "row-major"], default="packed",
                    help="weights of the W8A16 products: packed once at setup into the "
                         "kernel's fragment order (fp8_pack_w8a16_weights), or [N, K] rows")
@@ -125,55 +141,104 @@ def barrier(world: int):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 25 ms."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock, power and clock-event reasons of the benchmark's GPU,
+    sampled during the timed region.  NVML (libnvidia-ml, read-only queries)
+    every 2 ms; without NVML, nvidia-smi every 25 ms."""
+    NAMES = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+             0x4: "sw_power_cap"}
+    SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device):
-        self.samples = []
+    def __init__(self, device, period=0.002):
+        self.samples = []  # (time, sm_mhz, sm_max_mhz, power_w, [reason names])
+        self.period = period
+        self.source = None
         self.proc = None
         self.thread = None
-        self.gpu = self._gpu_id(device)
+        self.stop_flag = threading.Event()
+        self.bus = self._bus_id(device)
 
     @staticmethod
-    def _gpu_id(device):
+    def _bus_id(device):
         props = torch.cuda.get_device_properties(device)
         bus = getattr(props, "pci_bus_id", None)
-        dom = getattr(props, "pci_domain_id", 0)
-        devid = getattr(props, "pci_device_id", 0)
         if bus is None:
             return None
+        dom = getattr(props, "pci_domain_id", 0)
+        devid = getattr(props, "pci_device_id", 0)
         return f"{dom:08X}:{bus:02X}:{devid:02X}.0"
 
+    def _nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0 or self.bus is None:
+            return None
+        handle = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByPciBusId_v2(self.bus.encode(), ctypes.byref(handle)) != 0:
+            return None
+        reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        u, ull = ctypes.c_uint, ctypes.c_ulonglong
+
+        def sample():
+            sm, mx, pw, rs = u(), u(), u(), ull()
+            if (lib.nvmlDeviceGetClockInfo(handle, 1, ctypes.byref(sm)) != 0 or
+                    lib.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) != 0):
+                return None
+            power = pw.value / 1e3 if lib.nvmlDeviceGetPowerUsage(handle, ctypes.byref(pw)) == 0 else 0.0
+            names = ([n for bit, n in self.NAMES.items() if rs.value & bit]
+                     if reasons_fn(handle, ctypes.byref(rs)) == 0 else [])
+            return (time.perf_counter(), float(sm.value), float(mx.value), power, names)
+        return sample if sample() is not None else None
+
     def start(self):
-        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+        try:
+            sample = self._nvml()
+        except (OSError, AttributeError):
+            sample = None
+        if sample is not None:
+            self.source = f"nvml every {self.period * 1e3:.0f} ms"
+
+            def loop():
+                while not self.stop_flag.is_set():
+                    r = sample()
+                    if r is not None:
+                        self.samples.append(r)
+                    time.sleep(self.period)
+            self.thread = threading.Thread(target=loop, daemon=True)
+            self.thread.start()
+            return
+        cmd = ["nvidia-smi", f"--query-gpu={self.SMI_FIELDS}", "--format=csv,noheader,nounits",
                "-lms", "25"]
-        if self.gpu:
-            cmd += ["-i", self.gpu]
+        if self.bus:
+            cmd += ["-i", self.bus]
         try:
             self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
                                          text=True)
         except OSError:
-            self.proc = None
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.source = "nvidia-smi every 25 ms"
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+        def read():
+            for line in self.proc.stdout:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    self.samples.append((time.perf_counter(), float(parts[1]), float(parts[2]),
+                                         float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else 0.0,
+                                         [n for n, v in zip(names, parts[5:9])
+                                          if v.lower() == "active"]))
+                except ValueError:
+                    continue
+        self.thread = threading.Thread(target=read, daemon=True)
         self.thread.start()
         time.sleep(0.2)
 
-    def _read(self):
-        for line in self.proc.stdout:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                self.samples.append((time.perf_counter(), float(parts[1]), float(parts[2]),
-                                     float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else 0.0,
-                                     parts[5:9]))
-            except ValueError:
-                continue
-
     def stop(self):
+        self.stop_flag.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -183,22 +248,16 @@ class ClockSampler:
         if self.thread is not None:
             self.thread.join(timeout=5)
 
-    def summary(self, t0, t1, tw0):
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    def summary(self, t0, t1):
         inside = [s for s in self.samples if t0 <= s[0] <= t1]
-        window = "timed"
-        if len(inside) < 3:
-            inside = [s for s in self.samples if tw0 <= s[0] <= t1]
-            window = "warmup+timed"
         if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
-                    "window": window}
-        reasons = sorted({names[i] for s in inside for i, v in enumerate(s[4])
-                          if v.lower() == "active"})
+                    "source": self.source, "window": "timed"}
         return {"sm_mhz": float(np.median([s[1] for s in inside])),
                 "sm_max_mhz": float(max(s[2] for s in inside)),
-                "power_w_max": float(max(s[3] for s in inside)),
-                "reasons": reasons, "samples": len(inside), "window": window}
+                "power_w_max": round(float(max(s[3] for s in inside)), 1),
+                "reasons": sorted({n for s in inside for n in s[4]}),
+                "samples": len(inside), "source": self.source, "window": "timed"}
 
 
 # ----------------------------------------------------------------------------- workloads
@@ -220,7 +279,7 @@ class Call:
 
 
 class Workload:
-    def __init__(self, name, device, packed_w8a16=True):
+    def __init__(self, name, device, packed_w8a16=True, only_shape=None):
         import fp8_quantized_linear_gb300 as fl
         self.fl = fl
         self.name = name
@@ -229,12 +288,18 @@ class Workload:
         self.device = device
         self.copies = []      # per rotation copy: list of per-shape dicts
         self.rot = 1
+        self.shape_ids = (list(range(len(self.wl.shapes))) if only_shape is None
+                          else [only_shape])
+
+    def shapes(self):
+        """(index in the workload, (M, N, K)) of the shapes this run uses."""
+        return [(i, self.wl.shapes[i]) for i in self.shape_ids]
 
     # -- setup --
     def build(self):
         wl, dev, fl = self.wl, self.device, self.fl
         host = []
-        for i, (M, N, K) in enumerate(wl.shapes):
+        for i, (M, N, K) in self.shapes():
             seed = wl.seed(i)
             x = synthetic.activation(M, K, wl.x_dtype, seed=seed, outlier_frac=wl.outlier_frac)
             host.append((M, N, K, seed, x))
@@ -426,7 +491,7 @@ class Workload:
         oracle.build()
         jobs, units = [], 0
         if wl.kind == "w8a16":
-            for i, (M, N, K) in enumerate(wl.shapes):
+            for i, (M, N, K) in self.shapes():
                 seed = wl.seed(i)
                 n_s = min(N, max(16, int(N * fraction) // 16 * 16))
                 x = synthetic.activation(M, K, wl.x_dtype, seed=seed)
@@ -438,7 +503,7 @@ class Workload:
                     f"(brute-force C loops, 1 thread)")
             return jobs, units, desc
         rows = 8
-        for i, (M, N, K) in enumerate(wl.shapes):
+        for i, (M, N, K) in self.shapes():
             seed = wl.seed(i)
             r = min(rows, M)
             n_s = min(N, max(16, int(1024 * fraction) // 16 * 16))
@@ -639,13 +704,14 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     peaks = load_peaks()
-    work = Workload(args.workload, dev, packed_w8a16=args.w8a16_layout == "packed")
+    work = Workload(args.workload, dev, packed_w8a16=args.w8a16_layout == "packed",
+                    only_shape=args.only_shape)
     work.build()
     sampler = ClockSampler(dev)
     sampler.start()
     res = measure(work, args.steps, args.warmup, world)
     sampler.stop()
-    clocks = sampler.summary(res["window"][1], res["window"][2], res["window"][0])
+    clocks = sampler.summary(res["window"][1], res["window"][2])
     b, f = work.step_units()
     unit = work.headline_unit()
     value = aggregate(b if unit == "GB/s" else f, res["ms_per_step"], world, unit)
@@ -664,7 +730,7 @@ def run_ours(args):
                  else "e4m3 x e4m3 (fp32 accumulate)",
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights)",
         "config": {"workload": work.name, "description": work.wl.description,
-                   "shapes": [list(s) for s in work.wl.shapes],
+                   "shapes": [list(s) for _, s in work.shapes()],
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": (f"inputs larger than L2: {work.footprint / 2**20:.0f} MiB per step"
                           + (f" x {work.rot} rotating copies" if work.rot > 1 else "")),
@@ -686,13 +752,23 @@ def run_ours(args):
         "peaks": {k: peaks[k] for k in ("hbm_gbs", "bf16_tflops", "source")},
     }
     if rank == 0:
+        line["per_shape"] = per_shape(work, peaks, args.extra_steps)
+        line["per_shape_timing"] = ("each product alone: a CUDA graph of the call on R rotating "
+                                    "operand copies (together > 3x L2), replayed back to back "
+                                    "between CUDA events; frac = achieved / min(tensor peak, "
+                                    "HBM x AI)")
         jobs, units, desc = work.prepare_cpu_sample(1.0)
         secs = Workload.run_cpu_sample(jobs)
         cpu_val = (units / secs / 1e9) if unit == "GB/s" else (units / secs / 1e12)
         line["cpu_baseline"] = {"value": round(cpu_val, 6), "unit": unit, "cores": 1,
                                 "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
-        if not args.headline_only and work.name == "decode_w8a16":
+        shapes = [(work.name, line["per_shape"])]
+        if not args.headline_only and work.name == HEADLINE:
             line["workloads"] = other_workloads(args, dev, peaks)
+            shapes += [(e["workload"], e["per_shape"]) for e in line["workloads"]]
+            line["norm_fusion"] = norm_fusion_entry(dev, peaks, args.extra_steps)
+            line["decode_block"] = decode_block_entry(dev, peaks, args.extra_steps)
+        line["small_m"] = small_m_summary(shapes)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -700,58 +776,283 @@ def run_ours(args):
 
 
 def other_workloads(args, dev, peaks):
-    """Short measurements of the W8A8 workloads (summary entries)."""
+    """Short measurements of the other workloads (entries of the line)."""
     out = []
-    for name in ("prefill_w8a8_outliers", "llama3_8b_w8a8_sweep", "llama70b_static_fp8out"):
-        work = Workload(name, dev)
+    for name in ENTRY_WORKLOADS:
+        work = Workload(name, dev, packed_w8a16=args.w8a16_layout == "packed")
         work.build()
         res = measure(work, args.extra_steps, max(3, args.warmup // 2), 1)
         b, f = work.step_units()
+        unit = work.headline_unit()
         sec = res["ms_per_step"] / 1e3
         rf, kinds = roofline(res["per_kind"], peaks, res["ms_per_step"])
-        entry = {"workload": name, "value": round(f / sec / 1e12, 2), "unit": "TFLOP/s",
+        value = b / sec / 1e9 if unit == "GB/s" else f / sec / 1e12
+        entry = {"workload": name, "value": round(value, 2), "unit": unit,
                  "ms_per_step": round(res["ms_per_step"], 4), "steps": args.extra_steps,
-                 "roofline": rf, "kernels": kinds}
-        entry["per_shape"] = per_shape(work, args.extra_steps)
+                 "roofline": rf, "kernels": kinds,
+                 "per_shape": per_shape(work, peaks, args.extra_steps)}
         out.append(entry)
         del work
         torch.cuda.empty_cache()
     return out
 
 
-def per_shape(work, steps):
-    """Per-shape product times: eager calls bracketed by events, L2 flushed
-    before each timed call (the activation quantization of W8A8 shapes runs
-    untimed just before its product)."""
+def graph_time(fns, stream, reps):
+    """Seconds per replay of a CUDA graph of the calls `fns`, replayed `reps`
+    times back to back between two CUDA events on `stream`."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for fn in fns:
+            fn()
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            g.replay()
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        b.synchronize()
+    return a.elapsed_time(b) / 1e3 / reps
+
+
+def norm_fusion_entry(dev, peaks, steps, eps=1e-5):
+    """The prefill layer with its RMSNorm: per shape of the prefill workload
+    (M = 1024, K = 4096, 1% outlier channels), RMSNorm with the dynamic
+    per-tensor quantization fused into it (fp8_rmsnorm_quant) followed by the
+    product, against the unfused layer: RMSNorm writing bf16
+    (FP8L_NQ_NORM_ONLY), then the separate quantizer, then the product.
+    Inputs rotate over copies larger than 3x L2."""
+    import fp8_quantized_linear_gb300 as fl
+    wl = synthetic.WORKLOADS["prefill_w8a8_outliers"]
+    ws = fl.workspace(dev)
+    stream = torch.cuda.Stream(dev)
+    per_copy = sum(2 * M * K + M * K + N * K + 2 * M * N for (M, N, K) in wl.shapes)
+    n_rot = max(1, min(16, math.ceil(3 * L2_BYTES / per_copy)))
+    copies = []
+    for r in range(n_rot):
+        items = []
+        for i, (M, N, K) in enumerate(wl.shapes):
+            seed = wl.seed(i)
+            x = synthetic.activation(M, K, wl.x_dtype, seed=seed, outlier_frac=wl.outlier_frac)
+            w = synthetic.weight(N, K, torch.bfloat16, seed=seed).to(dev)
+            qw, sw = fl.fp8_quant_per_tensor(w)
+            items.append({"x": x.to(dev), "gamma": synthetic.norm_weight(K, wl.x_dtype, seed).to(dev),
+                          "qw": qw, "sw": sw, "h": torch.empty((M, K), dtype=wl.x_dtype, device=dev),
+                          "q": torch.empty((M, K), dtype=torch.uint8, device=dev),
+                          "s": torch.empty(1, dtype=torch.float32, device=dev),
+                          "y": torch.empty((M, N), dtype=torch.bfloat16, device=dev)})
+            del w
+        copies.append(items)
+
+    def fused():
+        return [lambda it=it: (fl.fp8_rmsnorm_quant(it["x"], it["gamma"], eps, q=it["q"],
+                                                    scale=it["s"], ws=ws),
+                               fl.fp8_scaled_mm(it["q"], it["qw"], it["s"], it["sw"], y=it["y"],
+                                                ws=ws, stable_weights=True))
+                for items in copies for it in items]
+
+    def unfused():
+        return [lambda it=it: (fl.fp8_rmsnorm_quant(it["x"], it["gamma"], eps, mode="norm_only",
+                                                    h=it["h"]),
+                               fl.fp8_quant_per_tensor(it["h"], q=it["q"], scale=it["s"], ws=ws),
+                               fl.fp8_scaled_mm(it["q"], it["qw"], it["s"], it["sw"], y=it["y"],
+                                                ws=ws, stable_weights=True))
+                for items in copies for it in items]
+
+    def norm_quant_only(fused_path):
+        if fused_path:
+            return [lambda it=it: fl.fp8_rmsnorm_quant(it["x"], it["gamma"], eps, q=it["q"],
+                                                       scale=it["s"], ws=ws)
+                    for items in copies for it in items]
+        return [lambda it=it: (fl.fp8_rmsnorm_quant(it["x"], it["gamma"], eps, mode="norm_only",
+                                                    h=it["h"]),
+                               fl.fp8_quant_per_tensor(it["h"], q=it["q"], scale=it["s"], ws=ws))
+                for items in copies for it in items]
+
+    with torch.cuda.stream(stream):
+        for fn in unfused() + fused():
+            fn()
+    stream.synchronize()
+    reps = max(3, min(50, steps))
+    t_f = graph_time(fused(), stream, reps) / n_rot
+    t_u = graph_time(unfused(), stream, reps) / n_rot
+    t_fq = graph_time(norm_quant_only(True), stream, reps) / n_rot
+    t_uq = graph_time(norm_quant_only(False), stream, reps) / n_rot
+    flops = sum(2 * M * N * K for (M, N, K) in wl.shapes)
+    nq_bytes = sum(3 * M * K + 2 * K + 4 for (M, N, K) in wl.shapes)  # x read, codes written
+    del copies
+    torch.cuda.empty_cache()
+    return {"workload": "prefill_w8a8_outliers with RMSNorm (eps 1e-5)",
+            "fused_step_us": round(t_f * 1e6, 2), "unfused_step_us": round(t_u * 1e6, 2),
+            "fused_TFLOP/s": round(flops / t_f / 1e12, 2),
+            "unfused_TFLOP/s": round(flops / t_u / 1e12, 2),
+            "speedup": round(t_u / t_f, 4),
+            "norm_quant_us": {"fused": round(t_fq * 1e6, 2), "unfused": round(t_uq * 1e6, 2)},
+            "fused_norm_quant_hbm_frac": round(nq_bytes / t_fq / 1e9 / peaks["hbm_gbs"], 4),
+            "timing": f"CUDA graph per variant over {n_rot} rotating copies, {reps} replays"}
+
+
+def decode_block_entry(dev, peaks, steps):
+    """The Llama-3-8B-shaped decode layer (fused q/k/v, o, fused gate/up,
+    down, each product reading the previous output) for M in {1, 16}: one
+    CUDA graph per layer replayed back to back, against the same calls
+    issued eagerly from Python.  Bytes per layer: the weights, scales and
+    16-bit activations each product reads and writes (the W8A8 layer adds
+    the quantizers' reads and writes)."""
+    from fp8_quantized_linear_gb300.block import ORDER, SHAPES, DecodeBlock
+    weights = {name: synthetic.weight(N, K, torch.bfloat16, seed=300 + i).to(dev)
+               for i, (name, (N, K)) in enumerate(SHAPES.items())}
+    stream = torch.cuda.Stream(dev)
+    reps = max(10, min(200, steps * 10))
+    out = []
+    for kind in ("w8a16", "w8a8"):
+        for M in (1, 16):
+            blk = DecodeBlock(M, weights, kind=kind)
+            blk.x.copy_(synthetic.activation(M, 4096, blk.act_dtype, seed=M).to(dev))
+            g = blk.capture(stream)
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    g.replay()
+                a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e.record(stream)
+                e.synchronize()
+                t_graph = a.elapsed_time(e) / 1e3 / reps
+                for _ in range(3):
+                    blk.forward()
+                stream.synchronize()
+                t0 = time.perf_counter()
+                a.record(stream)
+                for _ in range(reps):
+                    blk.forward()
+                e.record(stream)
+                e.synchronize()
+                t_eager = (time.perf_counter() - t0) / reps
+            nbytes = 0
+            for name in ORDER:
+                N, K = SHAPES[name]
+                if kind == "w8a16":
+                    nbytes += w8a16_bytes(M, N, K)
+                else:
+                    nbytes += w8a8_bytes(M, N, K, 2, True) + 3 * M * K
+            out.append({"kind": kind, "M": M, "graph_us": round(t_graph * 1e6, 2),
+                        "eager_us": round(t_eager * 1e6, 2),
+                        "graph_speedup": round(t_eager / t_graph, 3),
+                        "graph_GB/s": round(nbytes / t_graph / 1e9, 1),
+                        "graph_hbm_frac": round(nbytes / t_graph / 1e9 / peaks["hbm_gbs"], 4),
+                        "launches": blk.launches()})
+            del blk
+    del weights
+    torch.cuda.empty_cache()
+    return {"layer": "Llama-3-8B decode layer: qkv (6144,4096), o (4096,4096), gate_up "
+                     "(28672,4096), down (4096,14336), chained",
+            "timing": f"graph: {reps} replays between CUDA events; eager: the same calls from "
+                      "Python, wall time per layer",
+            "rows": out}
+
+
+def shape_roofline(flops, nbytes, seconds, peak_tflops, hbm_gbs):
+    """Figures of one product timed alone: achieved TFLOP/s and GB/s of
+    algorithmic units, the roofline min(tensor peak, HBM x arithmetic
+    intensity) with the bound that sets it, and the fractions of it and of
+    HBM bandwidth."""
+    tflops = flops / seconds / 1e12
+    gbs = nbytes / seconds / 1e9
+    mem_roof = hbm_gbs * (flops / nbytes) / 1e3  # TFLOP/s the bytes allow
+    roof = min(peak_tflops, mem_roof)
+    return {"TFLOP/s": round(tflops, 2), "GB/s": round(gbs, 1),
+            "bound": "hbm" if mem_roof < peak_tflops else "tensor",
+            "roof_TFLOP/s": round(roof, 1), "frac": round(tflops / roof, 4),
+            "hbm_frac": round(gbs / hbm_gbs, 4)}
+
+
+def per_shape(work, peaks, steps):
+    """Every shape's product timed alone.  For each shape, a CUDA graph holds
+    the one call on each of R copies of its operands (R such that the copies
+    exceed three L2 sizes, so each call reads from HBM), and is replayed back
+    to back between two CUDA events: no host dispatch or tensor-map encoding
+    falls inside the timed window.  W8A8 shapes also time their activation
+    quantization the same way.  The roofline of each product is
+    min(peak, HBM x AI): the FP8 tensor peak for W8A8, the 16-bit one for
+    W8A16."""
+    fl, wl, dev = work.fl, work.wl, work.device
+    ws = fl.workspace(dev)
+    stream = torch.cuda.Stream(dev)
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    reps = max(3, min(20, steps))
     rows = []
-    calls_by_copy = [work.calls(r) for r in range(work.rot)]
-    per = 1 if work.wl.kind == "w8a16" else 2
-    stream = torch.cuda.current_stream(work.device)
-    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=work.device)
-    reps = max(3, steps // 2)
-    for j in range(len(work.wl.shapes)):
-        tot_ms = 0.0
-        for rep in range(reps):
-            cc = calls_by_copy[rep % work.rot]
-            flush.zero_()
-            if per == 2:
-                cc[2 * j].fn()
+
+    def timed(fns):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for fn in fns:
+                fn()
+        with torch.cuda.stream(stream):
+            g.replay()
+            stream.synchronize()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            cc[per * j + per - 1].fn()
+            for _ in range(reps):
+                g.replay()
             b.record(stream)
             b.synchronize()
-            tot_ms += a.elapsed_time(b)
-        c = calls_by_copy[0][per * j + per - 1]
-        M, N, K = c.shape
-        ms = tot_ms / reps
-        row = {"M": M, "N": N, "K": K, "kernel": c.kind, "us": round(ms * 1e3, 2),
-               "TFLOP/s": round(2 * M * N * K / (ms / 1e3) / 1e12, 2)}
-        if c.unit == "bytes":
-            row["GB/s"] = round(c.units / (ms / 1e3) / 1e9, 1)
+        return a.elapsed_time(b) / 1e3 / (reps * len(fns))
+
+    for base in work.copies[0]:
+        M, N, K = base["M"], base["N"], base["K"]
+        if wl.kind == "w8a16":
+            nbytes, peak = w8a16_bytes(M, N, K), peaks["bf16_tflops"]
+            kind = "w8a16_skinny"
+        else:
+            nbytes = w8a8_bytes(M, N, K, base["y"].element_size(), wl.w_scale == "channel")
+            peak, kind = fp8_peak, "scaled_mm_skinny" if M <= 16 else "scaled_mm_tcgen05"
+        n_rot = max(1, min(64, math.ceil(3 * L2_BYTES / nbytes)))
+        copies = [base] + [{k: (v.clone() if isinstance(v, torch.Tensor) else v)
+                            for k, v in base.items()} for _ in range(n_rot - 1)]
+        if wl.kind == "w8a16":
+            prods = [lambda c=c: fl.fp8_w8a16_mm(c["x"], c["qw"], c["sw"], y=c["y"],
+                                                 stable_weights=True, packed=work.packed)
+                     for c in copies]
+            quants = []
+        else:
+            dyn = wl.act_scale == "dynamic"
+            quants = [lambda c=c: fl.fp8_quant_per_tensor(c["x"], q=c["qa"], scale=c["sa"],
+                                                          dynamic=dyn, ws=ws) for c in copies]
+            prods = [lambda c=c: fl.fp8_scaled_mm(c["qa"], c["qw"], c["sa"], c["sw"],
+                                                  out_dtype=c["y"].dtype, out_scale=c.get("os"),
+                                                  y=c["y"], ws=ws, stable_weights=True)
+                     for c in copies]
+        with torch.cuda.stream(stream):  # eager pass: quantized activations, library set-up
+            for fn in quants + prods:
+                fn()
+        stream.synchronize()
+        sec = timed(prods)
+        row = {"M": M, "N": N, "K": K, "kernel": kind, "us": round(sec * 1e6, 2),
+               **shape_roofline(2 * M * N * K, nbytes, sec, peak, peaks["hbm_gbs"]),
+               "copies": n_rot}
+        if quants:
+            qsec = timed(quants)
+            row["quant_us"] = round(qsec * 1e6, 2)
+            row["quant_hbm_frac"] = round(3 * M * K / qsec / 1e9 / peaks["hbm_gbs"], 4)
         rows.append(row)
-    del flush
+        del copies, prods, quants
+    torch.cuda.synchronize(dev)
     return rows
+
+
+def small_m_summary(lines):
+    """Which M <= 16 products reach HBM_TARGET of HBM bandwidth, timed alone."""
+    hit, miss = [], []
+    for wl_name, rows in lines:
+        for r in rows:
+            if r["M"] <= 16:
+                (hit if r["hbm_frac"] >= HBM_TARGET else miss).append(
+                    f"{wl_name} M={r['M']} N={r['N']} K={r['K']}: {r['hbm_frac']}")
+    return {"target_hbm_frac": HBM_TARGET, "at_or_above": hit, "below": miss}
 
 
 def run_reference(args):
@@ -764,6 +1065,8 @@ def run_reference(args):
     wl = synthetic.WORKLOADS[args.workload]
     work = Workload.__new__(Workload)
     work.wl, work.name = wl, args.workload
+    work.shape_ids = (list(range(len(wl.shapes))) if args.only_shape is None
+                      else [args.only_shape])
     unit = "GB/s" if wl.kind == "w8a16" else "TFLOP/s"
     probe_jobs, _, _ = work.prepare_cpu_sample(1.0 / 16)
     t_probe = Workload.run_cpu_sample(probe_jobs) * 16

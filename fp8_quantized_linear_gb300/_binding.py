@@ -78,6 +78,9 @@ def load():
         lib.fp8_packed_weight_bytes.argtypes = [I64, I64]
         lib.fp8_pack_w8a16_weights.restype = I
         lib.fp8_pack_w8a16_weights.argtypes = [P, I64, I64, P, P]
+        lib.fp8_grouped_mm.restype = I
+        lib.fp8_grouped_mm.argtypes = [P, P, P, I64, I64, I64, I64, P, P, I, P, P, I, P,
+                                       ctypes.c_uint, P]
         lib.fp8_rmsnorm_quant.restype = I
         lib.fp8_rmsnorm_quant.argtypes = [P, I, P, ctypes.c_float, I64, I64, P, P, I, P, P, P]
         _lib = lib
@@ -263,6 +266,45 @@ def fp8_scaled_mm(a: torch.Tensor, w: torch.Tensor, a_scale: torch.Tensor,
             per_channel, out_scale.data_ptr() if out_scale is not None else None,
             _codes(y).data_ptr(), code, ws.data_ptr(), flags, _stream(a.device))
     _check(st, "fp8_scaled_mm")
+    return y
+
+
+def fp8_grouped_mm(a: torch.Tensor, w: torch.Tensor, group_offsets: torch.Tensor,
+                   a_scale: torch.Tensor, w_scale: torch.Tensor, out_dtype=torch.bfloat16,
+                   out_scale: torch.Tensor | None = None, y: torch.Tensor | None = None,
+                   ws: torch.Tensor | None = None, stable_weights: bool = False,
+                   per_token: bool | None = None) -> torch.Tensor:
+    """Grouped W8A8 product of mixture-of-experts layers: rows
+    group_offsets[e] .. group_offsets[e+1]-1 of E4M3 a [M, K] times expert
+    e's E4M3 weights w[e] [N, K].  group_offsets: int32 [E + 1] on the
+    device; w_scale: [E] (per expert) or [E, N] (per channel); a_scale [1] or
+    [M] (per token).  Rows outside the groups of a freshly allocated y are
+    zero-filled first; a given y keeps them."""
+    _need_cuda(a, w, group_offsets, a_scale, w_scale, out_scale, y, ws)
+    a, w = _codes(a), _codes(w)
+    M, K = a.shape
+    E, N, K2 = w.shape
+    if K2 != K or group_offsets.numel() != E + 1 or group_offsets.dtype != torch.int32:
+        raise ValueError("shape mismatch")
+    per_channel = w_scale.numel() == E * N and N != 1
+    if w_scale.numel() not in (E, E * N):
+        raise ValueError("w_scale must have E or E * N entries")
+    if per_token is None:
+        per_token = a_scale.numel() == M and M > 1
+    if out_dtype == torch.float8_e4m3fn:
+        out_dtype = torch.uint8
+    if y is None:
+        y = torch.zeros((M, N), dtype=out_dtype, device=a.device)
+    if ws is None:
+        ws = workspace(a.device)
+    flags = (WEIGHTS_STABLE if stable_weights else 0) | (A_PER_TOKEN if per_token else 0)
+    with torch.cuda.device(a.device):
+        st = load().fp8_grouped_mm(
+            a.data_ptr(), w.data_ptr(), group_offsets.data_ptr(), E, M, N, K,
+            a_scale.data_ptr(), w_scale.data_ptr(), 1 if per_channel else 0,
+            out_scale.data_ptr() if out_scale is not None else None, _codes(y).data_ptr(),
+            _DTYPE_CODE[y.dtype], ws.data_ptr(), flags, _stream(a.device))
+    _check(st, "fp8_grouped_mm")
     return y
 
 

@@ -51,7 +51,12 @@ constexpr int kTmemCols = 2 * BN;  // two accumulators
 constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
 constexpr int kNumBarriers = 2 * STAGES + 2 + 2 + 1;
-constexpr size_t kSmemBytes = 1024 + size_t(STAGES) * kStageBytes + kNumBarriers * 8 + 16;
+constexpr int kMaxGroups = 256;  // grouped mode: experts
+// shared memory: alignment slack, stages, barriers, TMEM slot and abort flag
+// (16 bytes), then the grouped mode's row ranges and m-block prefix sums
+constexpr size_t kGroupSmemBytes = 3 * (kMaxGroups + 1) * sizeof(int);
+constexpr size_t kSmemBytes =
+    1024 + size_t(STAGES) * kStageBytes + kNumBarriers * 8 + 16 + kGroupSmemBytes;
 
 struct GemmParams {
     int M, N, K;
@@ -64,6 +69,9 @@ struct GemmParams {
     void *y;
     int out_dtype;
     unsigned *status;
+    const int *group_offs;  // grouped mode: [num_groups + 1] row offsets in device memory
+    int num_groups;         // 0: one product; > 0: expert e takes rows offs[e] .. offs[e+1]-1
+                            // and the weight rows e*N .. e*N + N-1 (w is [num_groups, N, K])
     long long wait_cycles;  // limit of the main waits (kDefaultWaitCycles unless a test shortened it)
     unsigned stall;         // kStallMma: testing the time-out path
     int split;  // > 1: a cluster of `split` CTAs shares one tile and splits its k-blocks
@@ -231,15 +239,17 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
 }
 
 // Scales and stores 32 accumulator columns [n0, n0+32) of row m; sa is the
-// row's activation scale and sa_sw = sa * w_scale[0].
+// row's activation scale, sa_sw = sa * (per-tensor weight scale) and wsc the
+// per-channel weight scales of the tile's weights (w_scale, or the expert's).
 __device__ __forceinline__ void store_row_chunk(const GemmParams &p, const uint32_t (&r)[32],
-                                                int m, int n0, float sa, float sa_sw) {
+                                                int m, int n0, float sa, float sa_sw,
+                                                const float *wsc) {
     const bool full32 = n0 + 32 <= p.N;  // N % 16 == 0: else exactly 16 columns remain
     float v[32];
     if (p.w_per_channel) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-            const float sw = (j < 16 || full32) ? __ldg(p.w_scale + n0 + j) : 0.0f;
+            const float sw = (j < 16 || full32) ? __ldg(wsc + n0 + j) : 0.0f;
             v[j] = __uint_as_float(r[j]) * (sa * sw);
         }
     } else {
@@ -272,6 +282,45 @@ __device__ __forceinline__ void store_row_chunk(const GemmParams &p, const uint3
             dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
         }
     }
+}
+
+// Where a tile sits: rows [row0, row_end) of A and Y (row_end bounds the
+// valid rows), weight rows from w_row0, output columns from n0, expert e.
+struct TileInfo {
+    int row0, row_end, w_row0, n0, e;
+};
+
+// Grouped mode: per expert the valid row range [lo, hi) (offsets clamped to
+// [0, M] and made non-decreasing) and the prefix sum of its 128-row blocks.
+struct GroupTable {
+    const int *lo, *hi, *prefix;  // shared memory; prefix has num_groups + 1 entries
+};
+
+__device__ __forceinline__ TileInfo tile_info(const GemmParams &p, const GroupTable &g, int tile,
+                                              int total_mb) {
+    TileInfo t;
+    const int mbg = tile % total_mb;
+    const int nb = tile / total_mb;
+    t.n0 = nb * BN;
+    if (p.num_groups == 0) {
+        t.row0 = mbg * BM;
+        t.row_end = p.M;
+        t.w_row0 = nb * BN;
+        t.e = 0;
+        return t;
+    }
+    // last expert whose first block is <= mbg (empty experts are skipped:
+    // their prefix equals the next one's)
+    int lo = 0, hi = p.num_groups;  // prefix[lo] <= mbg < prefix[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (g.prefix[mid] <= mbg) lo = mid; else hi = mid;
+    }
+    t.e = lo;
+    t.row0 = g.lo[lo] + (mbg - g.prefix[lo]) * BM;
+    t.row_end = g.hi[lo];
+    t.w_row0 = lo * p.N + nb * BN;
+    return t;
 }
 
 // Split mode: rows [rank*rows_per, ...) of the tile, summed over the cluster's
@@ -341,10 +390,36 @@ gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
     const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 4);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + STAGES * kStageBytes + kNumBarriers * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *g_lo = reinterpret_cast<int *>(gbase + STAGES * kStageBytes + kNumBarriers * 8 + 16);
+    int *g_hi = g_lo + (kMaxGroups + 1);
+    int *g_prefix = g_hi + (kMaxGroups + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    if (p.num_groups > 0) {
+        // expert row ranges from the device offsets, then the prefix sums of
+        // their 128-row blocks (one thread; at most kMaxGroups experts)
+        for (int e = threadIdx.x; e <= p.num_groups; e += blockDim.x) {
+            const int v = p.group_offs[e];
+            g_lo[e] = v < 0 ? 0 : (v > p.M ? p.M : v);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int run = 0, prev = 0;
+            for (int e = 0; e < p.num_groups; ++e) {
+                const int lo = g_lo[e] > prev ? g_lo[e] : prev;
+                int hi = g_lo[e + 1];
+                hi = hi > lo ? hi : lo;
+                g_prefix[e] = run;
+                run += (hi - lo + BM - 1) / BM;
+                g_lo[e] = lo;
+                g_hi[e] = hi;
+                prev = hi;
+            }
+            g_prefix[p.num_groups] = run;
+        }
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
@@ -371,7 +446,9 @@ gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int num_tiles = p.num_m_blocks * p.num_n_blocks;
+    const GroupTable gt{g_lo, g_hi, g_prefix};
+    const int total_mb = p.num_groups > 0 ? g_prefix[p.num_groups] : p.num_m_blocks;
+    const int num_tiles = total_mb * p.num_n_blocks;
     // persistent mode: tiles blockIdx.x, +gridDim.x, ...; split mode: the
     // cluster's one tile and this CTA's share of its k-blocks
     const bool split = p.split > 1;
@@ -394,8 +471,7 @@ gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
             uint32_t issued = 0, issued_parity = 0;  // per stage: load in flight, its parity
             bool ok = true;
             for (int tile = tile_begin; ok && tile < num_tiles; tile += tile_step) {
-                const int mb = tile % p.num_m_blocks;
-                const int nb = tile / p.num_m_blocks;
+                const TileInfo ti = tile_info(p, gt, tile, total_mb);
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.wait_cycles)) {
                         ok = false;
@@ -403,8 +479,8 @@ gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
                     }
                     const uint32_t sa = sbase + stage * kStageBytes;
                     mbar_expect_tx(full_bar(stage), kStageBytes);
-                    tma_load_2d(sa, &tmap_a, kb * BK, mb * BM, full_bar(stage));
-                    tma_load_2d(sa + kABytes, &tmap_b, kb * BK, nb * BN, full_bar(stage));
+                    tma_load_2d(sa, &tmap_a, kb * BK, ti.row0, full_bar(stage));
+                    tma_load_2d(sa + kABytes, &tmap_b, kb * BK, ti.w_row0, full_bar(stage));
                     issued |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -487,21 +563,23 @@ gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
             }
         }
         for (int tile = split ? num_tiles : tile_begin; tile < num_tiles; tile += tile_step) {
-            const int mb = tile % p.num_m_blocks;
-            const int nb = tile / p.num_m_blocks;
+            const TileInfo ti = tile_info(p, gt, tile, total_mb);
             if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status, p.wait_cycles)) break;
             tc_fence_after();
-            const int m = mb * BM + row;
-            const float sa = p.a_per_token ? (m < p.M ? __ldg(p.a_scale + m) : 0.0f) : sa0;
-            const float sa_sw = sa * sw0;
+            const int m = ti.row0 + row;
+            const bool row_ok = m < ti.row_end;
+            const float sa = p.a_per_token ? (row_ok ? __ldg(p.a_scale + m) : 0.0f) : sa0;
+            // grouped: the expert's scales (one, or N)
+            const float *wsc = p.w_scale + (p.w_per_channel ? static_cast<size_t>(ti.e) * p.N : ti.e);
+            const float sa_sw = sa * (p.num_groups > 0 && !p.w_per_channel ? __ldg(wsc) : sw0);
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld32(taddr + static_cast<uint32_t>(c * 32), r);
-                const int n0 = nb * BN + c * 32;
-                if (m < p.M && n0 < p.N) store_row_chunk(p, r, m, n0, sa, sa_sw);
+                const int n0 = ti.n0 + c * 32;
+                if (row_ok && n0 < p.N) store_row_chunk(p, r, m, n0, sa, sa_sw, wsc);
             }
             tc_fence_before();
             __syncwarp();
@@ -550,13 +628,16 @@ int ensure_smem_attr() {
     return FP8L_OK;
 }
 
+// groups == 0: one product of w [N, K]; groups > 0: w is [groups, N, K] and
+// group_offs the device row offsets of the experts (grouped mode).
 int launch_tcgen05(const uint8_t *a, const uint8_t *w, int M, int N, int K, const float *a_scale,
                    int a_per_token, const float *w_scale, int w_per_channel,
                    const float *out_scale, void *y,
-                   int out_dtype, unsigned *status, int sms, cudaStream_t stream) {
+                   int out_dtype, unsigned *status, int sms, cudaStream_t stream,
+                   const int *group_offs = nullptr, int groups = 0) {
     CUtensorMap ma, mb;
     if (make_map(&ma, a, M, K, BM) != FP8L_OK) return FP8L_ECUDA;
-    if (make_map(&mb, w, N, K, BN) != FP8L_OK) return FP8L_ECUDA;
+    if (make_map(&mb, w, int64_t(groups > 0 ? groups : 1) * N, K, BN) != FP8L_OK) return FP8L_ECUDA;
     if (ensure_smem_attr() != FP8L_OK) return FP8L_ECUDA;
     GemmParams p;
     p.M = M;
@@ -573,14 +654,17 @@ int launch_tcgen05(const uint8_t *a, const uint8_t *w, int M, int N, int K, cons
     p.y = y;
     p.out_dtype = out_dtype;
     p.status = status;
+    p.group_offs = group_offs;
+    p.num_groups = groups;
     const WaitConfig wc = wait_config();
     p.wait_cycles = wc.cycles;
     p.stall = wc.stall;
-    const int64_t tiles = int64_t(p.num_m_blocks) * p.num_n_blocks;
+    // grouped: each expert adds at most one partial block to ceil(M / BM)
+    const int64_t tiles = (int64_t(p.num_m_blocks) + groups) * p.num_n_blocks;
     // Few tiles (small M): a cluster of `split` CTAs per tile splits K so
     // that most SMs stream weights; otherwise one persistent CTA per SM.
     int split = 1;
-    if (tiles * 2 <= sms) {
+    if (groups == 0 && tiles * 2 <= sms) {
         split = static_cast<int>(sms / tiles);
         if (split > 8) split = 8;
         if (split > p.num_k_blocks) split = p.num_k_blocks;
@@ -640,4 +724,37 @@ extern "C" int fp8_scaled_mm(const uint8_t *a, const uint8_t *w, int64_t M, int6
     return launch_tcgen05(a, w, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
                           a_scale, pt, w_scale, pc, out_scale, y, out_dtype,
                           status_word(workspace), sms, s);
+}
+
+extern "C" int fp8_grouped_mm(const uint8_t *a, const uint8_t *w, const int32_t *group_offsets,
+                              int64_t num_groups, int64_t M, int64_t N, int64_t K,
+                              const float *a_scale, const float *w_scale, int w_per_channel,
+                              const float *out_scale, void *y, int out_dtype, void *workspace,
+                              unsigned flags, void *stream) {
+    using namespace fp8l;
+    if (out_dtype != FP8L_F16 && out_dtype != FP8L_BF16 && out_dtype != FP8L_E4M3)
+        return FP8L_EINVAL;
+    if ((flags & ~(FP8L_WEIGHTS_STABLE | FP8L_A_PER_TOKEN)) != 0u) return FP8L_EINVAL;
+    if (a_scale == nullptr || w_scale == nullptr || workspace == nullptr || w == nullptr ||
+        group_offsets == nullptr)
+        return FP8L_EINVAL;
+    if (out_dtype == FP8L_E4M3 && out_scale == nullptr) return FP8L_EINVAL;
+    if (num_groups < 1 || num_groups > kMaxGroups || M < 0 || M > 0x7FFFFFFF || N <= 0 ||
+        K <= 0 || N > (1 << 20) || K > (1 << 20) || N % 16 != 0 || K % 16 != 0 ||
+        num_groups * N > 0x7FFFFFFF)
+        return FP8L_ESHAPE;
+    if (M > 0 && (a == nullptr || y == nullptr)) return FP8L_EINVAL;
+    auto misaligned4 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) != 0; };
+    if (!aligned16(w) || !aligned16(workspace) || (M > 0 && (!aligned16(a) || !aligned16(y))) ||
+        misaligned4(a_scale) || misaligned4(w_scale) || misaligned4(group_offsets) ||
+        (out_dtype == FP8L_E4M3 && misaligned4(out_scale)))
+        return FP8L_EALIGN;
+    int sms = 0;
+    int st = check_device(&sms);
+    if (st != FP8L_OK) return st;
+    if (M == 0) return FP8L_OK;
+    return launch_tcgen05(a, w, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                          a_scale, (flags & FP8L_A_PER_TOKEN) != 0u ? 1 : 0, w_scale,
+                          w_per_channel ? 1 : 0, out_scale, y, out_dtype, status_word(workspace),
+                          sms, as_stream(stream), group_offsets, static_cast<int>(num_groups));
 }

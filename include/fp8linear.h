@@ -49,7 +49,7 @@ extern "C" {
 /* ABI version (fp8l_abi_version): 1, the first release; 2 adds
  * fp8_pack_w8a16_weights, fp8_packed_weight_bytes and FP8L_WEIGHTS_PACKED;
  * 3 adds fp8l_debug_waits, the per-token activation scales
- * (FP8L_A_PER_TOKEN) and fp8_rmsnorm_quant.  Each change is additive: a caller written for an
+ * (FP8L_A_PER_TOKEN), fp8_rmsnorm_quant and fp8_grouped_mm.  Each change is additive: a caller written for an
  * earlier version runs unchanged. */
 #define FP8L_ABI_VERSION 3
 
@@ -196,6 +196,37 @@ FP8L_API int fp8_scaled_mm(const uint8_t *a, const uint8_t *w, int64_t M, int64_
 FP8L_API int fp8_w8a16_mm(const void *x, int x_dtype, const uint8_t *w,
                  const float *w_scale, int64_t M, int64_t N, int64_t K,
                  void *y, unsigned flags, void *stream);
+
+/* Grouped W8A8 product for mixture-of-experts layers ("RFC: FP8
+ * Quantization Schema in vLLM", the gate_proj question: FP8 products need
+ * shapes divisible by 16; the experts' products are FP8, and a gate whose
+ * expert count is not a multiple of 16 is run through fp8_scaled_mm with
+ * its weights padded by zero rows to the next multiple of 16, the extra
+ * output columns then being exactly 0).  The tokens routed to expert e are
+ * the rows group_offsets[e] .. group_offsets[e+1]-1 of `a`:
+ *
+ *   y[m,n] = E(acc_e[m,n] * as(m) * ws_e(n))   for those rows, with
+ *   acc_e[m,n] = sum_k dec(a[m,k]) * dec(w[e][n,k])   (fp32 accumulation)
+ *   ws_e(n) = w_scale[e*N + n] when w_per_channel, else w_scale[e];
+ *   as(m) and the output cast E() as in fp8_scaled_mm.
+ *
+ * a: [M, K] E4M3 codes (rows sorted by expert); w: [num_groups, N, K] E4M3
+ * codes; group_offsets: num_groups + 1 int32 in DEVICE memory (written by
+ * the routing step, read by the kernel, so no host round trip), with
+ * 0 <= offsets[0] <= offsets[1] <= ... <= offsets[num_groups] <= M; rows
+ * outside [offsets[0], offsets[num_groups]) are not written (values are
+ * clamped to [0, M] and made non-decreasing).  a_scale: 1 float, or M with
+ * FP8L_A_PER_TOKEN; w_scale: num_groups floats, or num_groups * N with
+ * w_per_channel; out_scale and out_dtype as in fp8_scaled_mm.
+ * 1 <= num_groups <= 256; N, K positive multiples of 16 at most 2^20;
+ * num_groups * N < 2^31; 0 <= M <= 2^31 - 1.  Runs the tcgen05 kernel with
+ * one persistent CTA per SM whatever the group sizes.  workspace: status
+ * word.  flags: any of FP8L_WEIGHTS_STABLE and FP8L_A_PER_TOKEN. */
+FP8L_API int fp8_grouped_mm(const uint8_t *a, const uint8_t *w, const int32_t *group_offsets,
+                            int64_t num_groups, int64_t M, int64_t N, int64_t K,
+                            const float *a_scale, const float *w_scale, int w_per_channel,
+                            const float *out_scale, void *y, int out_dtype, void *workspace,
+                            unsigned flags, void *stream);
 
 /* Size in bytes of the packed layout of an [N, K] E4M3 weight tensor:
  * N * ceil(K / 64) * 64.  Returns 0 when N or K is not a positive multiple

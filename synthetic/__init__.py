@@ -78,6 +78,12 @@ def weight(N: int, K: int, dtype: torch.dtype, seed: int,
     return normal_matrix(N, K, 0.02, dtype, seed + 500_000, row_subset=row_subset)
 
 
+def norm_weight(K: int, dtype: torch.dtype, seed: int) -> torch.Tensor:
+    """RMSNorm gain gamma [K] ~ N(1, 0.1^2)."""
+    g = torch.Generator().manual_seed(_block_seed(seed, 777_777))
+    return (1.0 + 0.1 * torch.randn(K, generator=g, dtype=torch.float32)).to(dtype)
+
+
 @dataclass(frozen=True)
 class Workload:
     name: str

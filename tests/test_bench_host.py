@@ -116,3 +116,43 @@ def test_reference_arm_prints_one_line_on_rank_0_only(monkeypatch, capsys):
     assert line["config"]["workload"] == "tiny_w8a8"
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_per_shape_roofline_is_the_lower_of_tensor_peak_and_bandwidth():
+    # M = 64, N = K = 8192 E4M3 with E4M3 output and per-channel scales:
+    # AI = 2MNK / bytes ~ 124 flop/B, so 6807.9 GB/s allows ~845 TFLOP/s,
+    # below the 3812.6 TFLOP/s peak: bound by HBM
+    M, N, K = 64, 8192, 8192
+    nbytes = bench.w8a8_bytes(M, N, K, 1, True)
+    flops = 2 * M * N * K
+    r = bench.shape_roofline(flops, nbytes, 30e-6, 3812.6, 6807.9)
+    mem_roof = 6807.9 * flops / nbytes / 1e3
+    assert r["bound"] == "hbm"
+    assert r["roof_TFLOP/s"] == pytest.approx(mem_roof, abs=0.05)
+    assert r["frac"] == pytest.approx(flops / 30e-6 / 1e12 / mem_roof, abs=1e-4)
+    assert r["hbm_frac"] == pytest.approx(nbytes / 30e-6 / 1e9 / 6807.9, abs=1e-4)
+    # M = 4096: compute-bound, the roofline is the tensor peak
+    M = 4096
+    nbytes = bench.w8a8_bytes(M, N, K, 1, True)
+    r = bench.shape_roofline(2 * M * N * K, nbytes, 200e-6, 3812.6, 6807.9)
+    assert r["bound"] == "tensor" and r["roof_TFLOP/s"] == 3812.6
+    assert r["frac"] == pytest.approx(2 * M * N * K / 200e-6 / 1e12 / 3812.6, abs=1e-4)
+
+
+def test_small_m_summary_splits_at_the_target():
+    rows = [{"M": 1, "N": 16, "K": 16, "hbm_frac": 0.71},
+            {"M": 16, "N": 32, "K": 16, "hbm_frac": 0.69},
+            {"M": 64, "N": 32, "K": 16, "hbm_frac": 0.10}]
+    s = bench.small_m_summary([("w", rows)])
+    assert s["target_hbm_frac"] == 0.70
+    assert s["at_or_above"] == ["w M=1 N=16 K=16: 0.71"]
+    assert s["below"] == ["w M=16 N=32 K=16: 0.69"]
+
+
+def test_default_workload_is_the_largest():
+    args = bench.parse_args([])
+    assert args.workload == "llama70b_static_fp8out"
+    import synthetic
+    flops = {n: sum(2 * m * n_ * k for (m, n_, k) in w.shapes)
+             for n, w in synthetic.WORKLOADS.items()}
+    assert max(flops, key=flops.get) == args.workload

@@ -86,6 +86,58 @@ def test_static_every_16bit_value(dtype, scale):
     assert np.array_equal(host(q).reshape(-1), q_o.reshape(-1))
 
 
+def _many_scales():
+    """The fast-path limits of the kernels' quotient (2^-92 and 2^100) and
+    their float32 neighbours on both sides, other landmarks (subnormal and
+    huge scales, reciprocals that are not exact), and 256 seeded scales with
+    random significands and exponents in [-100, 100]."""
+    f32 = np.float32
+    lims = [f32(2.0 ** -92), f32(2.0 ** 100)]
+    out = []
+    for v in lims:
+        out += [np.nextafter(v, f32(0)), v, np.nextafter(v, f32(np.inf))]
+    out += [f32(2.0 ** -93), f32(2.0 ** 101), f32(2.0 ** -126), f32(1e-40), f32(3e38),
+            f32(1.0), f32(0.1), f32(1.0 / 3.0), f32(7.0), f32(1.0 / 448.0), f32(2.0 ** -9),
+            f32(448.0)]
+    rng = np.random.default_rng(2024)
+    sig = rng.integers(0, 1 << 23, 256, dtype=np.uint32)
+    exp = rng.integers(-100, 101, 256)
+    out += list(((((127 + exp) << 23).astype(np.uint32)) | sig).view(np.float32))
+    return [f32(v) for v in out]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_static_every_16bit_value_many_scales(dtype):
+    # every finite value of the format under 274 scales: the kernels' codes
+    # (corrected quotient, or IEEE division outside [2^-92, 2^100]) against
+    # the oracle's IEEE division, bit for bit
+    v = torch.from_numpy(pins.all_16bit_values(dtype)).to(dtype)
+    x = v.reshape(1, -1)
+    xd = dev(x)
+    for s in _many_scales():
+        q, _ = fl.fp8_quant_per_tensor(xd, scale=scalar(s), dynamic=False)
+        q_o, _ = oracle.quant_per_tensor(x, scale=s)
+        assert np.array_equal(host(q).reshape(-1), q_o.reshape(-1)), (dtype, float(s))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_dynamic_every_16bit_value_below_an_amax(dtype):
+    # dynamic mode: the finite values of the format up to a chosen maximum A
+    # (both signs), for 48 maxima of various exponents and significands; the
+    # scale RN(A / 448) and every code must equal the oracle's
+    v = pins.all_16bit_values(dtype)
+    pos = np.unique(np.abs(v[np.isfinite(v)]))
+    rng = np.random.default_rng(7)
+    picks = np.concatenate([pos[-1:], pos[rng.integers(len(pos) // 4, len(pos) - 1, 47)]])
+    for a in picks:
+        sel = v[np.abs(v) <= a]
+        x = torch.from_numpy(sel).to(dtype).reshape(1, -1)
+        q, s = fl.fp8_quant_per_tensor(dev(x))
+        q_o, s_o = oracle.quant_per_tensor(x)
+        assert np.float32(host(s)[0]) == s_o, (dtype, float(a))
+        assert np.array_equal(host(q).reshape(-1), q_o.reshape(-1)), (dtype, float(a))
+
+
 def test_static_float32_midpoint_neighbourhoods():
     # every E4M3 rounding midpoint and 64 float32 neighbours on each side
     table = oracle.decode_table()
