@@ -22,6 +22,7 @@ F16, BF16, E4M3, F32 = 0, 1, 2, 3
 WEIGHTS_STABLE = 1
 WEIGHTS_PACKED = 2
 A_PER_TOKEN = 4
+SINGLE_SM_TILES = 8
 OK, EINVAL, ESHAPE, EALIGN, ECUDA, ETIMEOUT, EUNSUPPORTED = range(7)
 
 _DTYPE_CODE = {torch.float16: F16, torch.bfloat16: BF16, torch.float32: F32,
@@ -232,13 +233,13 @@ def fp8_scaled_mm(a: torch.Tensor, w: torch.Tensor, a_scale: torch.Tensor,
                   w_scale: torch.Tensor, out_dtype=torch.bfloat16,
                   out_scale: torch.Tensor | None = None, y: torch.Tensor | None = None,
                   ws: torch.Tensor | None = None, stable_weights: bool = False,
-                  per_token: bool | None = None) -> torch.Tensor:
+                  per_token: bool | None = None, single_sm: bool = False) -> torch.Tensor:
     """W8A8 product of E4M3 a [M, K] and w [N, K] with a per-tensor ([1]) or
     per-token ([M]) a_scale and a per-tensor ([1]) or per-channel ([N])
     w_scale.  out_dtype bf16 / fp16, or uint8 (E4M3 codes, needs out_scale).
     stable_weights sets FP8L_WEIGHTS_STABLE (no work in flight on the stream
     writes w or w_scale); per_token (default: a_scale has M > 1 entries) sets
-    FP8L_A_PER_TOKEN."""
+    FP8L_A_PER_TOKEN; single_sm sets FP8L_SINGLE_SM_TILES."""
     _need_cuda(a, w, a_scale, w_scale, out_scale, y, ws)
     a, w = _codes(a), _codes(w)
     M, K = a.shape
@@ -259,7 +260,8 @@ def fp8_scaled_mm(a: torch.Tensor, w: torch.Tensor, a_scale: torch.Tensor,
         per_token = a_scale.numel() == M and M > 1
     if a_scale.numel() != (M if per_token else 1):
         raise ValueError("a_scale must have 1 entry, or M with per_token")
-    flags = (WEIGHTS_STABLE if stable_weights else 0) | (A_PER_TOKEN if per_token else 0)
+    flags = ((WEIGHTS_STABLE if stable_weights else 0) | (A_PER_TOKEN if per_token else 0) |
+             (SINGLE_SM_TILES if single_sm else 0))
     with torch.cuda.device(a.device):
         st = load().fp8_scaled_mm(
             a.data_ptr(), w.data_ptr(), M, N, K, a_scale.data_ptr(), w_scale.data_ptr(),

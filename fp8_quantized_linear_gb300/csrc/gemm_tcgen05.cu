@@ -107,21 +107,48 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 // Bounded wait for the phase of parity `parity`.  Gives up when another
 // role raised the abort flag, or after `limit` cycles (then raises it and
 // records the time-out).
+// In a CTA pair (peer_abort != 0, the peer's flag as a shared::cluster
+// address) a time-out raises the peer's flag too, and the wait acquires at
+// cluster scope (the barrier may be completed by the peer CTA).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                       unsigned *status, long long limit) {
-    if (mbar_try_wait(bar, parity)) return true;
+                                       unsigned *status, long long limit, uint32_t peer_abort = 0) {
+    auto ready = [&]() { return peer_abort ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (ready()) return true;
     const long long t0 = clock64();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (ready()) return true;
         if ((i & 63u) == 0u) {
             if (*abort_flag) return false;
             if (clock64() - t0 > limit) {
                 *abort_flag = 1;
+                if (peer_abort)
+                    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_abort), "r"(1) : "memory");
                 atomicOr(status, kStatusTimeout);
                 return false;
             }
         }
     }
+}
+
+// The common case first: one test of the phase inline, the bounded loop only
+// when it is not complete yet (keeps the MMA issue loop short).
+__device__ __forceinline__ bool mbar_wait_fast(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                               unsigned *status, long long limit,
+                                               uint32_t peer_abort = 0) {
+    if (peer_abort ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    return mbar_wait(bar, parity, abort_flag, status, limit, peer_abort);
 }
 
 // Bounded wait used while tearing down: ignores the abort flag.
@@ -184,27 +211,16 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
         : "memory");
 }
 
+// shared::cluster address of `local` (a shared::cta address) in CTA `rank`
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ float4 ld_cluster_v4(uint32_t local_addr, uint32_t rank) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(remote)
-                 : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -238,6 +254,34 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
         __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
 }
 
+// E4M3 output codes of v / output_scale.  The quotient is the correctly
+// rounded RN(v / os) without a division: with y = RN(1/os), q0 = RN(v y) and
+// two corrections q <- RN(q + RN(v - os q) y) (fused multiply-adds), the
+// second of which is correctly rounded by Markstein's theorem (P. Markstein,
+// IBM J. Res. Develop. 34(1), 1990) when the residual does not underflow and
+// nothing overflows.  That holds for 2^-92 <= os <= 2^100 once |v| is
+// clamped to 1024 os (every code from 464 os up saturates to 448 anyway);
+// other output scales take the IEEE division.
+struct OutDiv {
+    float os, y, cap;
+    bool fast;
+    __device__ __forceinline__ static OutDiv make(float os) {
+        OutDiv d;
+        d.os = os;
+        d.y = __frcp_rn(os);
+        d.cap = 1024.0f * os;
+        d.fast = os >= 0x1p-92f && os <= 0x1p100f;
+        return d;
+    }
+    __device__ __forceinline__ float quot(float v) const {
+        if (!fast) return __fdiv_rn(v, os);
+        const float vc = copysignf(fminf(fabsf(v), cap), v);
+        float q = __fmul_rn(vc, y);
+        q = __fmaf_rn(__fmaf_rn(-os, q, vc), y, q);
+        return __fmaf_rn(__fmaf_rn(-os, q, vc), y, q);
+    }
+};
+
 // Scales and stores 32 accumulator columns [n0, n0+32) of row m; sa is the
 // row's activation scale, sa_sw = sa * (per-tensor weight scale) and wsc the
 // per-channel weight scales of the tile's weights (w_scale, or the expert's).
@@ -257,12 +301,12 @@ __device__ __forceinline__ void store_row_chunk(const GemmParams &p, const uint3
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * sa_sw;
     }
     if (p.out_dtype == FP8L_E4M3) {
-        const float os = __ldg(p.out_scale);
+        const OutDiv d = OutDiv::make(__ldg(p.out_scale));
         uint32_t w[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const uint32_t lo = e4m3x2(__fdiv_rn(v[4 * i], os), __fdiv_rn(v[4 * i + 1], os));
-            const uint32_t hi = e4m3x2(__fdiv_rn(v[4 * i + 2], os), __fdiv_rn(v[4 * i + 3], os));
+            const uint32_t lo = e4m3x2(d.quot(v[4 * i]), d.quot(v[4 * i + 1]));
+            const uint32_t hi = e4m3x2(d.quot(v[4 * i + 2]), d.quot(v[4 * i + 3]));
             w[i] = lo | (hi << 16);
         }
         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.y) +
@@ -323,11 +367,33 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, const GroupTa
     return t;
 }
 
-// Split mode: rows [rank*rows_per, ...) of the tile, summed over the cluster's
-// partial tiles (distributed shared memory), scaled, cast and stored; four
+// Split mode: every CTA of the cluster writes its fp32 partial tile into its
+// own (idle) stage ring, row pitch kPartPitch floats; after a cluster
+// barrier CTA `rank` adds the `split` partials of its rows [rank*rows_per,
+// ...) read through distributed shared memory (all `split` loads of a group
+// of four columns issued before any is used), scales, casts and stores: four
 // columns per thread, consecutive threads on consecutive columns.
 constexpr int kPartPitch = BN + 4;  // floats per partial-tile row (conflict-free v4 stores)
+constexpr int kMaxSplit = 8;
 static_assert(BM * kPartPitch * 4 <= STAGES * kStageBytes, "partial tile fits in the ring");
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// v4 load from CTA `rank`'s shared memory at this CTA's offset `local_addr`
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t local_addr, uint32_t rank) {
+    const uint32_t remote = map_to_rank(local_addr, rank);
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(remote)
+                 : "memory");
+    return v;
+}
 
 __device__ void split_reduce_store(const GemmParams &p, int tile, int rank, uint32_t sbase) {
     const int mb = tile % p.num_m_blocks;
@@ -345,13 +411,19 @@ __device__ void split_reduce_store(const GemmParams &p, int tile, int rank, uint
         const int n = nb * BN + col;
         if (m >= p.M || n >= p.N) continue;
         const uint32_t off = sbase + static_cast<uint32_t>((row * kPartPitch + col) * 4);
+        float4 part[kMaxSplit];
+#pragma unroll
+        for (int q = 0; q < kMaxSplit; ++q)
+            if (q < p.split) part[q] = ld_cluster_v4(off, static_cast<uint32_t>(q));
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int q = 0; q < p.split; ++q) {
-            const float4 v = ld_cluster_v4(off, static_cast<uint32_t>(q));
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+#pragma unroll
+        for (int q = 0; q < kMaxSplit; ++q) {  // the same order in every run
+            if (q < p.split) {
+                acc.x += part[q].x;
+                acc.y += part[q].y;
+                acc.z += part[q].z;
+                acc.w += part[q].w;
+            }
         }
         float v[4] = {acc.x, acc.y, acc.z, acc.w};
         const float sa = p.a_per_token ? __ldg(p.a_scale + m) : sa0;
@@ -359,9 +431,9 @@ __device__ void split_reduce_store(const GemmParams &p, int tile, int rank, uint
         for (int j = 0; j < 4; ++j)
             v[j] *= sa * (p.w_per_channel ? __ldg(p.w_scale + n + j) : sw0);
         if (p.out_dtype == FP8L_E4M3) {
-            const float os = __ldg(p.out_scale);
-            const uint32_t lo = e4m3x2(__fdiv_rn(v[0], os), __fdiv_rn(v[1], os));
-            const uint32_t hi = e4m3x2(__fdiv_rn(v[2], os), __fdiv_rn(v[3], os));
+            const OutDiv d = OutDiv::make(__ldg(p.out_scale));
+            const uint32_t lo = e4m3x2(d.quot(v[0]), d.quot(v[1]));
+            const uint32_t hi = e4m3x2(d.quot(v[2]), d.quot(v[3]));
             *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(p.y) + static_cast<size_t>(m) * p.N + n) =
                 lo | (hi << 16);
         } else {
@@ -378,6 +450,10 @@ __device__ void split_reduce_store(const GemmParams &p, int tile, int rank, uint
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
                 const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+    // launched as a programmatic dependent (stable weights), the kernel is
+    // resident before the preceding kernel ends; it touches no global memory
+    // until that kernel's writes are visible (a no-op otherwise)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;  // swizzle atoms need 1024-byte alignment
@@ -509,17 +585,18 @@ gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
-                    if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status, p.wait_cycles)) {
+                    if (!mbar_wait_fast(full_bar(stage), phase, abort_flag, p.status, p.wait_cycles)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t sa = sbase + stage * kStageBytes;
-                    const uint32_t sb = sa + kABytes;
+                    // descriptors of the stage's operands; k step: +32 bytes = +2
+                    // in the start-address field (addresses >> 4)
+                    const uint64_t da = sw128_desc(sa), db = sw128_desc(sa + kABytes);
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k)
-                        mma_f8(d_tmem, sw128_desc(sa + k * UMMA_K), sw128_desc(sb + k * UMMA_K),
-                               ((kb - kb_begin) | k) != 0 ? 1u : 0u);
+                        mma_f8(d_tmem, da + 2 * k, db + 2 * k, ((kb - kb_begin) | k) != 0 ? 1u : 0u);
                     mma_commit(empty_bar(stage));  // stage reusable once these MMAs retire
                     if (++stage == STAGES) {
                         stage = 0;
@@ -544,8 +621,7 @@ gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
         int acc = 0;
         uint32_t acc_phase = 0;
         if (split) {
-            // fp32 partial tile into the (now idle) stage ring: part[row][col],
-            // row pitch kPartPitch floats
+            // fp32 partial tile into the (now idle) stage ring: part[row][col]
             if (mbar_wait(tfull_bar(0), 0, abort_flag, p.status, p.wait_cycles)) {
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -607,6 +683,274 @@ gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
     }
 }
 
+
+// ---------------------------------------------------------------- CTA-pair kernel
+//
+// The same product with the tile split over a pair of SMs (a cluster of two
+// CTAs): tcgen05.mma.cta_group::2 computes a 256 x 256 tile per k-step, each
+// CTA staging 128 rows of A and 128 rows (half of the tile's columns) of W;
+// the MMA reads the peer's operand halves from its shared memory, and each
+// CTA's TMEM receives its 128 rows of the accumulator.  Per SM and k-block
+// that is 32 KB of operands for the same 128 x 256 x 128 of MMA work that
+// costs 48 KB in the single-SM kernel, so six stages fit where four did and
+// the loads run further ahead of the tensor pipe.
+//   warp 0     TMA producer in each CTA: its own A and W halves; both CTAs'
+//              copies complete on the even CTA's full barrier, armed by the
+//              even CTA for the bytes of both.
+//   warp 1     TMEM (512 columns, allocated by both CTAs together); in the
+//              even CTA one lane issues the MMAs, and its commits arrive on
+//              the stage-empty and accumulator-full barriers of both CTAs.
+//   warps 2-5  epilogue in each CTA over its 128 rows; the accumulator-empty
+//              barrier in the even CTA collects the 8 epilogue warps of the
+//              pair.
+// Waits are bounded as in the single-SM kernel; a time-out also raises the
+// peer's abort flag, and both CTAs meet at a cluster barrier before TMEM is
+// released.
+constexpr int P_BM = 128;                            // rows per CTA; a pair covers 256
+constexpr int P_BN = 256;                            // MMA N; each CTA stages half of it
+constexpr int P_STAGES = 6;
+constexpr int kPABytes = P_BM * BK;                  // 16 KB
+constexpr int kPBBytes = (P_BN / 2) * BK;            // 16 KB
+constexpr int kPStageBytes = kPABytes + kPBBytes;    // 32 KB
+constexpr int kPNumBarriers = 2 * P_STAGES + 2 + 2 + 1;
+constexpr size_t kPSmemBytes = 1024 + size_t(P_STAGES) * kPStageBytes + kPNumBarriers * 8 + 16;
+// kind::f8f6f4, D f32, A and B E4M3 K-major, N = 256, M = 256 (pair)
+constexpr uint32_t kIdescPair = (1u << 4) | (uint32_t(P_BN >> 3) << 17) | (uint32_t(256 >> 4) << 24);
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// TMA load into this CTA's shared memory, completing on an mbarrier of
+// either CTA of the pair (bar: shared::cluster address)
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                                 uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(kIdescPair), "r"(accumulate)
+        : "memory");
+}
+
+// arrive on the barrier at this offset in both CTAs once the MMAs issued so
+// far have retired
+__device__ __forceinline__ void commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(static_cast<uint16_t>(3))
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_f8_pair(const __grid_constant__ CUtensorMap tmap_a,
+             const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // see gemm_f8_tcgen05
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (sbase - raw);
+    const uint32_t bar0 = sbase + P_STAGES * kPStageBytes;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (P_STAGES + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * P_STAGES + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * P_STAGES + 2 + b); };
+    const uint32_t done_bar = bar0 + 8u * (2 * P_STAGES + 4);
+    uint32_t *tmem_slot =
+        reinterpret_cast<uint32_t *>(gbase + P_STAGES * kPStageBytes + kPNumBarriers * 8);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P_STAGES; ++s) {
+            mbar_init(full_bar(s), 1);   // the even CTA's arming arrival (+ both CTAs' bytes)
+            mbar_init(empty_bar(s), 1);  // the MMA commit, multicast to both CTAs
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), 2 * kEpiWarps);  // the pair's epilogue warps
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // both CTAs' barriers exist before either touches the other's
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t peer_abort = map_to_rank(smem_u32(const_cast<int *>(abort_flag)), rank ^ 1u);
+
+    const int pair = static_cast<int>(blockIdx.x) >> 1;
+    const int num_pairs = static_cast<int>(gridDim.x) >> 1;
+    const int tiles_m = (p.M + 2 * P_BM - 1) / (2 * P_BM);
+    const int num_tiles = tiles_m * p.num_n_blocks;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed = 0, armed_parity = 0;  // even CTA: stages armed, their parity
+            bool ok = true;
+            for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
+                const int mt = tile % tiles_m;
+                const int nt = tile / tiles_m;
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.wait_cycles,
+                                   peer_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = sbase + stage * kPStageBytes;
+                    if (leader) {
+                        mbar_expect_tx(full_bar(stage), 2 * kPStageBytes);
+                        armed |= 1u << stage;
+                        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    }
+                    const uint32_t fb = map_to_rank(full_bar(stage), 0);
+                    tma_load_2d_pair(sa, &tmap_a, kb * BK, mt * 2 * P_BM + static_cast<int>(rank) * P_BM, fb);
+                    tma_load_2d_pair(sa + kPABytes, &tmap_b, kb * BK,
+                                     nt * P_BN + static_cast<int>(rank) * (P_BN / 2), fb);
+                    if (++stage == P_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // the even CTA's full barriers count both CTAs' copies: every
+            // armed stage lands before either CTA passes the final cluster
+            // barrier
+            for (int s = 0; s < P_STAGES; ++s)
+                if (armed & (1u << s)) mbar_wait_drain(full_bar(s), (armed_parity >> s) & 1u, p.status);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            if (p.stall & kStallMma)
+                ok = mbar_wait(done_bar, 0, abort_flag, p.status, p.wait_cycles, peer_abort);
+            for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
+                if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status, p.wait_cycles,
+                               peer_abort))
+                    break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * P_BN);
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!mbar_wait_fast(full_bar(stage), phase, abort_flag, p.status, p.wait_cycles,
+                                        peer_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = sbase + stage * kPStageBytes;
+                    const uint64_t da = sw128_desc(sa), db = sw128_desc(sa + kPABytes);
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; ++k)
+                        mma_f8_pair(d_tmem, da + 2 * k, db + 2 * k, (kb | k) != 0 ? 1u : 0u);
+                    commit_pair(empty_bar(stage));
+                    if (++stage == P_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                commit_pair(tfull_bar(acc));
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            // every MMA issued has retired (all tcgen05 operations of this
+            // kernel use the pair form; the peer's copy of the barrier is unused)
+            commit_pair(done_bar);
+            mbar_wait_drain(done_bar, 0, p.status);
+        }
+        __syncwarp();
+    } else {
+        const int quarter = warp & 3;
+        const int row = static_cast<int>(rank) * P_BM + quarter * 32 + lane;  // row in the pair tile
+        const float sa0 = __ldg(p.a_scale);
+        const float sw0 = __ldg(p.w_scale);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = pair; tile < num_tiles; tile += num_pairs) {
+            const int mt = tile % tiles_m;
+            const int nt = tile / tiles_m;
+            if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status, p.wait_cycles, peer_abort))
+                break;
+            tc_fence_after();
+            const int m = mt * 2 * P_BM + row;
+            const bool row_ok = m < p.M;
+            const float sa = p.a_per_token ? (row_ok ? __ldg(p.a_scale + m) : 0.0f) : sa0;
+            const float sa_sw = sa * sw0;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   static_cast<uint32_t>(acc * P_BN);
+#pragma unroll 1
+            for (int c = 0; c < P_BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(taddr + static_cast<uint32_t>(c * 32), r);
+                const int n0 = nt * P_BN + c * 32;
+                if (row_ok && n0 < p.N) store_row_chunk(p, r, m, n0, sa, sa_sw, p.w_scale);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader)
+                    mbar_arrive(tempty_bar(acc));
+                else
+                    mbar_arrive_remote(map_to_rank(tempty_bar(acc), 0));
+            }
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    // every copy, MMA and TMEM read of the pair is finished before TMEM is
+    // released and before either CTA's shared memory goes away
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
 // ---------------------------------------------------------------- host side
 
 // 2-D map over a row-major [rows, K] uint8 matrix, box BK x box_rows, 128B swizzle
@@ -622,22 +966,30 @@ int ensure_smem_attr() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP8L_ECUDA;
     if (g_smem_set[dev].load(std::memory_order_acquire)) return FP8L_OK;
     if (cudaFuncSetAttribute(gemm_f8_tcgen05, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes)) != cudaSuccess)
+                             static_cast<int>(kSmemBytes)) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_f8_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kPSmemBytes)) != cudaSuccess)
         return FP8L_ECUDA;
     g_smem_set[dev].store(1, std::memory_order_release);
     return FP8L_OK;
 }
 
 // groups == 0: one product of w [N, K]; groups > 0: w is [groups, N, K] and
-// group_offs the device row offsets of the experts (grouped mode).
+// group_offs the device row offsets of the experts (grouped mode).  Products
+// with enough tiles to fill the SMs run the CTA-pair kernel unless
+// single_sm; grouped products and small-M split-K run the single-SM kernel.
 int launch_tcgen05(const uint8_t *a, const uint8_t *w, int M, int N, int K, const float *a_scale,
                    int a_per_token, const float *w_scale, int w_per_channel,
                    const float *out_scale, void *y,
                    int out_dtype, unsigned *status, int sms, cudaStream_t stream,
-                   const int *group_offs = nullptr, int groups = 0) {
+                   const int *group_offs = nullptr, int groups = 0, bool single_sm = false,
+                   bool pdl = false) {
     CUtensorMap ma, mb;
+    const bool pair_ok = groups == 0 && !single_sm && sms >= 2 &&
+                         int64_t((M + BM - 1) / BM) * ((N + BN - 1) / BN) * 2 > sms;
     if (make_map(&ma, a, M, K, BM) != FP8L_OK) return FP8L_ECUDA;
-    if (make_map(&mb, w, int64_t(groups > 0 ? groups : 1) * N, K, BN) != FP8L_OK) return FP8L_ECUDA;
+    if (make_map(&mb, w, int64_t(groups > 0 ? groups : 1) * N, K, pair_ok ? P_BN / 2 : BN) != FP8L_OK)
+        return FP8L_ECUDA;
     if (ensure_smem_attr() != FP8L_OK) return FP8L_ECUDA;
     GemmParams p;
     p.M = M;
@@ -659,6 +1011,27 @@ int launch_tcgen05(const uint8_t *a, const uint8_t *w, int M, int N, int K, cons
     const WaitConfig wc = wait_config();
     p.wait_cycles = wc.cycles;
     p.stall = wc.stall;
+    if (pair_ok) {
+        const int64_t pair_tiles = int64_t((M + 2 * P_BM - 1) / (2 * P_BM)) * p.num_n_blocks;
+        const int64_t pairs = pair_tiles < sms / 2 ? pair_tiles : sms / 2;
+        p.split = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kPSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = pdl ? 2 : 1;
+        if (cudaLaunchKernelEx(&cfg, gemm_f8_pair, ma, mb, p) != cudaSuccess) return FP8L_ECUDA;
+        return launch_status();
+    }
     // grouped: each expert adds at most one partial block to ceil(M / BM)
     const int64_t tiles = (int64_t(p.num_m_blocks) + groups) * p.num_n_blocks;
     // Few tiles (small M): a cluster of `split` CTAs per tile splits K so
@@ -666,7 +1039,7 @@ int launch_tcgen05(const uint8_t *a, const uint8_t *w, int M, int N, int K, cons
     int split = 1;
     if (groups == 0 && tiles * 2 <= sms) {
         split = static_cast<int>(sms / tiles);
-        if (split > 8) split = 8;
+        if (split > kMaxSplit) split = kMaxSplit;
         if (split > p.num_k_blocks) split = p.num_k_blocks;
         if (split < 1) split = 1;
     }
@@ -676,13 +1049,22 @@ int launch_tcgen05(const uint8_t *a, const uint8_t *w, int M, int N, int K, cons
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(split);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    int nattr = 0;
+    if (split > 1) {
+        attr[nattr].id = cudaLaunchAttributeClusterDimension;
+        attr[nattr].val.clusterDim.x = static_cast<unsigned>(split);
+        attr[nattr].val.clusterDim.y = 1;
+        attr[nattr].val.clusterDim.z = 1;
+        ++nattr;
+    }
+    if (pdl) {
+        attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+        ++nattr;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = split > 1 ? 1 : 0;
+    cfg.numAttrs = nattr;
     if (cudaLaunchKernelEx(&cfg, gemm_f8_tcgen05, ma, mb, p) != cudaSuccess) return FP8L_ECUDA;
     return launch_status();
 }
@@ -697,7 +1079,8 @@ extern "C" int fp8_scaled_mm(const uint8_t *a, const uint8_t *w, int64_t M, int6
     using namespace fp8l;
     if (out_dtype != FP8L_F16 && out_dtype != FP8L_BF16 && out_dtype != FP8L_E4M3)
         return FP8L_EINVAL;
-    if ((flags & ~(FP8L_WEIGHTS_STABLE | FP8L_A_PER_TOKEN)) != 0u) return FP8L_EINVAL;
+    if ((flags & ~(FP8L_WEIGHTS_STABLE | FP8L_A_PER_TOKEN | FP8L_SINGLE_SM_TILES)) != 0u)
+        return FP8L_EINVAL;
     if (a_scale == nullptr || w_scale == nullptr || workspace == nullptr || w == nullptr)
         return FP8L_EINVAL;
     if (out_dtype == FP8L_E4M3 && out_scale == nullptr) return FP8L_EINVAL;
@@ -723,7 +1106,9 @@ extern "C" int fp8_scaled_mm(const uint8_t *a, const uint8_t *w, int64_t M, int6
                                   out_dtype, (flags & FP8L_WEIGHTS_STABLE) != 0u, s);
     return launch_tcgen05(a, w, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
                           a_scale, pt, w_scale, pc, out_scale, y, out_dtype,
-                          status_word(workspace), sms, s);
+                          status_word(workspace), sms, s, nullptr, 0,
+                          (flags & FP8L_SINGLE_SM_TILES) != 0u,
+                          (flags & FP8L_WEIGHTS_STABLE) != 0u);
 }
 
 extern "C" int fp8_grouped_mm(const uint8_t *a, const uint8_t *w, const int32_t *group_offsets,
@@ -756,5 +1141,6 @@ extern "C" int fp8_grouped_mm(const uint8_t *a, const uint8_t *w, const int32_t 
     return launch_tcgen05(a, w, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
                           a_scale, (flags & FP8L_A_PER_TOKEN) != 0u ? 1 : 0, w_scale,
                           w_per_channel ? 1 : 0, out_scale, y, out_dtype, status_word(workspace),
-                          sms, as_stream(stream), group_offsets, static_cast<int>(num_groups));
+                          sms, as_stream(stream), group_offsets, static_cast<int>(num_groups), false,
+                          (flags & FP8L_WEIGHTS_STABLE) != 0u);
 }

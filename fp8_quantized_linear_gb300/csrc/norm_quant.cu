@@ -62,50 +62,69 @@ __device__ __forceinline__ uint32_t to_16x2(float a, float b) {
     }
 }
 
-// h word (8 elements) of x word xv and gamma word gv
 template <int DT>
-__device__ __forceinline__ uint4 norm_word(const uint4 &xv, const uint4 &gv, float r) {
+__device__ __forceinline__ uint64_t to_pair(uint32_t w) {
+    const float2 f = to_float2<DT>(w);
+    return f2_pack(__float_as_uint(f.x), __float_as_uint(f.y));
+}
+
+// h word (8 elements) of x word xv and gamma word gv: RN16((x * r) * gamma),
+// two products on float pairs
+template <int DT>
+__device__ __forceinline__ uint4 norm_word(const uint4 &xv, const uint4 &gv, uint64_t r2) {
     const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
     const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
     uint32_t hw[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float2 xf = to_float2<DT>(xw[i]);
-        const float2 gf = to_float2<DT>(gw[i]);
-        hw[i] = to_16x2<DT>(__fmul_rn(__fmul_rn(xf.x, r), gf.x), __fmul_rn(__fmul_rn(xf.y, r), gf.y));
+        const uint64_t h = f2_mul(f2_mul(to_pair<DT>(xw[i]), r2), to_pair<DT>(gw[i]));
+        hw[i] = to_16x2<DT>(__uint_as_float(static_cast<uint32_t>(h)),
+                            __uint_as_float(static_cast<uint32_t>(h >> 32)));
     }
     return make_uint4(hw[0], hw[1], hw[2], hw[3]);
 }
 
-// sum of squares of the 8 elements of a word, added to acc (x^2 is exact in
-// float32 for 16-bit x)
+// squares of the 8 elements of a word added to a pair of partial sums (x^2 is
+// exact in float32 for 16-bit x)
 template <int DT>
-__device__ __forceinline__ float word_sumsq(const uint4 &xv, float acc) {
+__device__ __forceinline__ uint64_t word_sumsq(const uint4 &xv, uint64_t acc) {
     const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float2 f = to_float2<DT>(xw[i]);
-        acc = __fmaf_rn(f.x, f.x, acc);
-        acc = __fmaf_rn(f.y, f.y, acc);
+        const uint64_t f = to_pair<DT>(xw[i]);
+        acc = f2_fma(f, f, acc);
     }
     return acc;
 }
 
-// sum over the block; every thread gets the result (fixed order)
-__device__ __forceinline__ float block_sum(float v, float *red) {
+// Sum over the block with one barrier: warp sums go to buffer `flip` of red,
+// then every thread adds the 16 warp sums in the same order.  Alternating
+// the buffer between calls keeps a call's writes clear of the previous
+// call's reads (every thread has passed this call's barrier by then).
+__device__ __forceinline__ float block_sum(float v, float (*red)[kNThreads / 32], int &flip) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) red[warp] = v;
+    if (lane == 0) red[flip][warp] = v;
     __syncthreads();
-    if (warp == 0) {
-        float t = lane < (kNThreads >> 5) ? red[lane] : 0.0f;
+    float t = 0.0f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
-        if (lane == 0) red[32] = t;
-    }
+    for (int i = 0; i < kNThreads / 32; ++i) t += red[flip][i];
+    flip ^= 1;
+    return t;
+}
+
+// the same for a maximum of magnitude bits
+__device__ __forceinline__ uint32_t block_max(uint32_t v, uint32_t (*red)[kNThreads / 32], int &flip) {
+    v = __reduce_max_sync(0xFFFFFFFFu, v);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[flip][warp] = v;
     __syncthreads();
-    return red[32];
+    uint32_t t = 0;
+#pragma unroll
+    for (int i = 0; i < kNThreads / 32; ++i) t = max(t, red[flip][i]);
+    flip ^= 1;
+    return t;
 }
 
 struct NormArgs {
@@ -127,11 +146,15 @@ template <int DT, int NW>
 __global__ void __launch_bounds__(kNThreads, 1) rmsnorm_quant_kernel(const NormArgs a) {
     extern __shared__ __align__(128) uint4 rows_smem[];
     __shared__ __align__(8) uint64_t full[kNormMaxStages];
-    __shared__ float fred[33];
-    __shared__ uint32_t ured[33];
+    __shared__ float fred[2][kNThreads / 32];
+    __shared__ uint32_t ured[2][kNThreads / 32];
+    __shared__ uint32_t bred[33];
     __shared__ int abort_sh;
     __shared__ unsigned epoch_sh;
 
+    // a product launched as a programmatic dependent may be scheduled now;
+    // it waits for this grid's writes itself
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x;
     const int G = static_cast<int>(gridDim.x);
     const int b = static_cast<int>(blockIdx.x);
@@ -178,34 +201,35 @@ __global__ void __launch_bounds__(kNThreads, 1) rmsnorm_quant_kernel(const NormA
                   keep ? l2_evict_last() : l2_evict_first());
         pending |= 1u << s;
     };
-    // thread 0 waits (bounded) for stage s; the block barrier releases the
-    // others.  False for every thread after a time-out.
+    // every thread waits (bounded) for stage s itself; a time-out is noted in
+    // abort_sh and acted on after the next block barrier, which keeps the
+    // barriers uniform
     auto wait_stage = [&](int s) {
-        if (tid == 0) {
-            if (q_mbar_wait(smem_u32(&full[s]), (par >> s) & 1u, a.wait_cycles))
-                pending &= ~(1u << s);
-            else
-                abort_sh = 1;
-        }
-        __syncthreads();
-        if (abort_sh) return false;
+        if (!q_mbar_wait(smem_u32(&full[s]), (par >> s) & 1u, a.wait_cycles))
+            abort_sh = 1;
+        else if (tid == 0)
+            pending &= ~(1u << s);
         par ^= 1u << s;
-        return true;
     };
-    // the row's x words into registers and r; after the block sum every
-    // thread has read the stage, so thread 0 may refill it
+    // the row's x words into registers and r = 1 / sqrt(ss / K + eps); after
+    // the block sum every thread has read the stage, so thread 0 may refill
+    // it
+    int fflip = 0, uflip = 0;
     uint4 xv[NW];
     auto load_row = [&](int s) {
         const uint4 *src = rows_smem + static_cast<size_t>(s) * words;
-        float acc = 0.0f;
+        uint64_t acc = 0;
 #pragma unroll
         for (int j = 0; j < NW; ++j) {
             const int w = tid + j * kNThreads;
             xv[j] = w < words ? src[w] : make_uint4(0, 0, 0, 0);
             acc = word_sumsq<DT>(xv[j], acc);
         }
-        const float ss = block_sum(acc, fred);
-        return __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(a.K)), a.eps)));
+        const float part = __fadd_rn(__uint_as_float(static_cast<uint32_t>(acc)),
+                                     __uint_as_float(static_cast<uint32_t>(acc >> 32)));
+        const float ss = block_sum(part, fred, fflip);
+        const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(a.K)), a.eps)));
+        return f2_pack(__float_as_uint(r), __float_as_uint(r));
     };
     auto store_row = [&](int row, const uint4 (&hv)[NW], const Quot *d, bool clamp) {
         const size_t base = static_cast<size_t>(row) * words;
@@ -230,21 +254,32 @@ __global__ void __launch_bounds__(kNThreads, 1) rmsnorm_quant_kernel(const NormA
     // ---- pass 1 (the only pass except in dynamic mode)
     for (int i = 0; i < n; ++i) {
         const int s = i % S;
-        if (!wait_stage(s)) goto teardown;
-        const float r = load_row(s);
+        wait_stage(s);
+        const uint64_t r2 = load_row(s);
+        if (abort_sh) goto teardown;
         if (tid == 0 && i + S < n) issue(i + S, s, dyn && i + S < first_res);
         const int row = b + G * i;
         uint4 hv[NW];
         uint32_t m = 0;
 #pragma unroll
         for (int j = 0; j < NW; ++j) {
-            hv[j] = norm_word<DT>(xv[j], gw[j], r);
+            hv[j] = norm_word<DT>(xv[j], gw[j], r2);
             m = word_mag_max<DT>(hv[j], m);  // zero words beyond the row add nothing
         }
         if (dyn) {
             m_all = max(m_all, fold_mag<DT>(m));  // m holds two 16-bit maxima
+            if (i >= first_res) {
+                // a row that stays on chip keeps h in place of x (each thread
+                // rewrites only its own words): pass 2 only casts it
+                uint4 *dst = rows_smem + static_cast<size_t>(s) * words;
+#pragma unroll
+                for (int j = 0; j < NW; ++j) {
+                    const int w = tid + j * kNThreads;
+                    if (w < words) dst[w] = hv[j];
+                }
+            }
         } else if (a.mode == kNqPerToken) {
-            const uint32_t rm = block_max_u32(fold_mag<DT>(m), ured);
+            const uint32_t rm = block_max(fold_mag<DT>(m), ured, uflip);
             const float sc = scale_from_amax(mag_bits_to_float<DT>(rm));
             if (tid == 0) a.scale[row] = sc;
             const Quot d = Quot::make<DT>(sc);
@@ -258,28 +293,47 @@ __global__ void __launch_bounds__(kNThreads, 1) rmsnorm_quant_kernel(const NormA
     }
     if (!dyn) return;
     {
-        // ---- grid maximum, then pass 2: resident rows first, then the rest
-        const uint32_t bm = block_max_u32(fold_mag<DT>(m_all), ured);
+        // ---- grid maximum, then pass 2: resident rows first (h already in
+        // shared memory), then the others, re-read and normalized again
+        const uint32_t bm = block_max_u32(fold_mag<DT>(m_all), bred);
         const unsigned pair = epoch_sh & 1u;
+        // a single block has the maximum already and skips the barrier words
+        const bool barrier = G > 1 || (a.stall & kStallGrid) != 0u;
         const unsigned expect = gridDim.x + ((a.stall & kStallGrid) ? 1u : 0u);
-        uint32_t mm;
-        if (!grid_max(a.arrive + pair, a.amax + pair, bm, a.status, &mm, expect, a.wait_cycles))
+        uint32_t mm = bm;
+        if (barrier && !grid_max(a.arrive + pair, a.amax + pair, bm, a.status, &mm, expect, a.wait_cycles))
             return;  // every copy of pass 1 was waited for
         const float sc = scale_from_amax(mag_bits_to_float<DT>(mm));
         if (b == 0 && tid == 0) {
             *a.scale = sc;
-            *a.epoch = epoch_sh + 1u;
+            if (barrier) *a.epoch = epoch_sh + 1u;
         }
         const Quot d = Quot::make<DT>(sc);
         for (int j = 0; j < n; ++j) {
-            const int idx = j < n_res ? first_res + j : j - n_res;
             const int s = (first_res + j) % S;
-            if (j >= n_res && !wait_stage(s)) goto teardown;
-            const float r = load_row(s);
-            if (tid == 0 && j + S < n) issue(j + S - n_res, s, false);
             uint4 hv[NW];
+            int idx;
+            if (j < n_res) {
+                idx = first_res + j;
+                const uint4 *src = rows_smem + static_cast<size_t>(s) * words;
 #pragma unroll
-            for (int jj = 0; jj < NW; ++jj) hv[jj] = norm_word<DT>(xv[jj], gw[jj], r);
+                for (int jj = 0; jj < NW; ++jj) {
+                    const int w = tid + jj * kNThreads;
+                    hv[jj] = w < words ? src[w] : make_uint4(0, 0, 0, 0);
+                }
+                if (j + S < n) {
+                    __syncthreads();  // every thread has read the stage
+                    if (tid == 0) issue(j + S - n_res, s, false);
+                }
+            } else {
+                idx = j - n_res;
+                wait_stage(s);
+                const uint64_t r2 = load_row(s);
+                if (abort_sh) goto teardown;
+                if (tid == 0 && j + S < n) issue(j + S - n_res, s, false);
+#pragma unroll
+                for (int jj = 0; jj < NW; ++jj) hv[jj] = norm_word<DT>(xv[jj], gw[jj], r2);
+            }
             store_row(b + G * idx, hv, &d, false);
         }
         return;

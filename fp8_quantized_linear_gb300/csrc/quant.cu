@@ -215,6 +215,9 @@ quant_tma_kernel(const void *__restrict__ x, int64_t numel, uint8_t *__restrict_
     __shared__ unsigned epoch_sh;
     constexpr int EB = Elt<DT>::kBytes;
     constexpr int EPW = 16 / EB;  // elements per 16-byte word
+    // a product launched as a programmatic dependent may be scheduled now;
+    // it waits for this grid's writes itself
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x;
     const int G = static_cast<int>(gridDim.x);
     const int b = static_cast<int>(blockIdx.x);
@@ -312,15 +315,17 @@ quant_tma_kernel(const void *__restrict__ x, int64_t numel, uint8_t *__restrict_
             goto teardown;
         }
         const unsigned pair = epoch_sh & 1u;
-        uint32_t mm;
+        uint32_t mm = m;
+        // a single block has the maximum already and skips the barrier words
         // (testing the time-out path: one arrival more than the grid has)
+        const bool barrier = G > 1 || (stall & kStallGrid) != 0u;
         const unsigned expect = gridDim.x + ((stall & kStallGrid) ? 1u : 0u);
-        if (!grid_max(arrive + pair, amax + pair, m, status, &mm, expect, wait_cycles))
+        if (barrier && !grid_max(arrive + pair, amax + pair, m, status, &mm, expect, wait_cycles))
             return;  // no copy in flight here
         sc = scale_from_amax(mag_bits_to_float<DT>(mm));
         if (blockIdx.x == 0 && tid == 0) {
             *scale = sc;
-            *epoch = epoch_sh + 1u;  // every block read the counter before arriving
+            if (barrier) *epoch = epoch_sh + 1u;  // every block read the counter before arriving
         }
         first_res = npieces > stages ? npieces - stages : 0;
         n_res = npieces - first_res;

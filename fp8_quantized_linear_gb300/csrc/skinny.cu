@@ -304,7 +304,7 @@ int launch_nt(const SkinnyArgs &a, bool stable_weights, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = stable_weights ? 1 : 0;
-    constexpr int unroll = (NT == 1 && PACKED) ? kUnrollPacked1 : kUnroll;
+    constexpr int unroll = (NT == 1 && (PACKED || XK == kXE4M3)) ? kUnrollPacked1 : kUnroll;
     if (cudaLaunchKernelEx(&cfg, skinny_kernel<XK, NT, kWarps, unroll, PACKED>, a) != cudaSuccess)
         return FP8L_ECUDA;
     return launch_status();

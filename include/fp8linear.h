@@ -78,10 +78,11 @@ enum fp8l_status {
  * FP8L_WEIGHTS_STABLE: the caller guarantees that no work still in flight on
  * `stream` writes the weights `w` or the weight scales (the usual case of an
  * inference loop, where weights are written once at load time).  The
- * weight-streaming kernel is then launched as a programmatic dependent of
- * the preceding kernel on the stream and issues its first weight loads
- * before waiting for that kernel, so consecutive products overlap.
- * Activations, scales and outputs are still only accessed after the wait. */
+ * product's kernel is then launched as a programmatic dependent of the
+ * preceding kernel on the stream, so it is resident before that kernel
+ * ends; the weight-streaming kernel also issues its first weight loads
+ * before waiting for it, so consecutive products overlap.  Activations,
+ * scales and outputs are only accessed after the wait. */
 #define FP8L_WEIGHTS_STABLE 1u
 
 /* FP8L_WEIGHTS_PACKED (fp8_w8a16_mm only): `w` holds the weights in the
@@ -92,6 +93,13 @@ enum fp8l_status {
  * row of `a` (per-token activation scales, as fp8_quant_per_row computes
  * them for activations), instead of one. */
 #define FP8L_A_PER_TOKEN 4u
+
+/* FP8L_SINGLE_SM_TILES (fp8_scaled_mm only): run a tensor-core product
+ * with one SM per 128 x 256 tile even where it would pair two SMs on a
+ * 256 x 256 tile (a tuning and testing option; both kernels accumulate in
+ * fp32 over k in the same blocks, and their results agree within the
+ * layer's tolerance). */
+#define FP8L_SINGLE_SM_TILES 8u
 
 /* Element types. */
 enum fp8l_dtype {
@@ -170,10 +178,13 @@ FP8L_API int fp8_quant_per_row(const void *x, int x_dtype, int64_t rows, int64_t
  * when out_dtype is FP8L_E4M3 and ignored otherwise.
  * M >= 0 (M == 0 launches nothing); N and K are positive multiples of 16
  * (the FP8 GEMM shape rule), N, K <= 2^20, M <= 2^31 - 1.
- * M <= 16 runs a weight-streaming kernel; larger M runs the tcgen05 tensor
- * core kernel.  workspace: fp8l_workspace_bytes() bytes (status word).
- * flags: any of FP8L_WEIGHTS_STABLE and FP8L_A_PER_TOKEN (other bits are
- * FP8L_EINVAL). */
+ * M <= 16 runs a weight-streaming kernel; larger M runs a tcgen05 tensor
+ * core kernel: clusters of CTAs splitting K when the tiles are few, else a
+ * persistent kernel whose 256 x 256 tiles each span a pair of SMs
+ * (tcgen05.mma.cta_group::2), or 128 x 256 tiles on one SM each with
+ * FP8L_SINGLE_SM_TILES.  workspace: fp8l_workspace_bytes() bytes (status word).
+ * flags: any of FP8L_WEIGHTS_STABLE, FP8L_A_PER_TOKEN and
+ * FP8L_SINGLE_SM_TILES (other bits are FP8L_EINVAL). */
 FP8L_API int fp8_scaled_mm(const uint8_t *a, const uint8_t *w, int64_t M, int64_t N,
                   int64_t K, const float *a_scale, const float *w_scale,
                   int w_per_channel, const float *out_scale, void *y,

@@ -156,3 +156,17 @@ def test_default_workload_is_the_largest():
     flops = {n: sum(2 * m * n_ * k for (m, n_, k) in w.shapes)
              for n, w in synthetic.WORKLOADS.items()}
     assert max(flops, key=flops.get) == args.workload
+
+
+def test_long_timed_regions_use_the_sustained_tensor_peak():
+    peaks = {"hbm_gbs": 6807.9, "bf16_tflops": 1951.8, "bf16_tflops_sustained": 1690.5,
+             "source": "measured"}
+    per_kind = {"scaled_mm_tcgen05": {"ms": 1.0, "units_per_step": 3e12, "unit": "flops",
+                                      "launches_per_step": 12}}
+    burst, _ = bench.roofline(per_kind, peaks, ms_per_step=1.0)
+    sust, _ = bench.roofline(per_kind, peaks, ms_per_step=1.0, sustained=True)
+    assert burst["peak"] == pytest.approx(3903.6) and sust["peak"] == pytest.approx(3381.0)
+    assert burst["frac"] == burst["frac_of_burst"] == pytest.approx(3000 / 3903.6, abs=1e-4)
+    assert sust["frac"] == pytest.approx(3000 / 3381.0, abs=1e-4)
+    assert sust["frac_of_burst"] == burst["frac"]
+    assert "sustained" in sust["peak_source"] and "burst" in burst["peak_source"]
