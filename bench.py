@@ -684,11 +684,20 @@ KERNEL_SOURCES = {"w8a16_skinny": "skinny.cu", "scaled_mm_skinny": "skinny.cu",
 
 
 def kernel_source_hash(src):
-    """sha256 prefix of a kernel's translation unit followed by the shared
-    header it includes (a change to either invalidates a capture)."""
+    """sha256 prefix of a kernel's translation unit followed by the library
+    headers it includes, directly or through another one (a change to any of
+    them invalidates a capture)."""
     csrc = os.path.join(ROOT, "fp8_quantized_linear_gb300", "csrc")
+    order, todo = [], [src]
+    while todo:
+        name = todo.pop(0)
+        if name in order or not os.path.exists(os.path.join(csrc, name)):
+            continue
+        order.append(name)
+        with open(os.path.join(csrc, name)) as f:
+            todo += re.findall(r'^#include "([^"]+)"', f.read(), flags=re.M)
     h = hashlib.sha256()
-    for name in (src, "common.cuh"):
+    for name in order:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -374,7 +374,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, const GroupTa
 // of four columns issued before any is used), scales, casts and stores: four
 // columns per thread, consecutive threads on consecutive columns.
 constexpr int kPartPitch = BN + 4;  // floats per partial-tile row (conflict-free v4 stores)
-constexpr int kMaxSplit = 8;
+constexpr int kMaxSplit = 4;  // clusters of 8 at this shared-memory size ran 1.4-1.7x slower
 static_assert(BM * kPartPitch * 4 <= STAGES * kStageBytes, "partial tile fits in the ring");
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,

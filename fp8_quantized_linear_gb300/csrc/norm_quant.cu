@@ -35,9 +35,11 @@
 namespace fp8l {
 namespace {
 
-constexpr int kNThreads = 512;
-constexpr int kNormMaxK = 32768;                 // 8 words of 8 elements per thread
-constexpr int kNormSmemBudget = 200 * 1024;      // bytes of row stages per CTA
+// 256 threads per block for K <= 8192 (up to four blocks per SM, so one
+// block's per-row barriers overlap the others' work), 512 above; a thread
+// holds at most 8 words (64 elements) of a row
+constexpr int kNormMaxK = 32768;
+constexpr int kNormSmemBudget = 200 * 1024;      // bytes of row stages per SM
 constexpr int kNormMaxStages = 32;
 
 enum NqMode { kNqDynamic = 0, kNqStatic = 1, kNqPerToken = 2, kNqNormOnly = 3 };
@@ -101,7 +103,8 @@ __device__ __forceinline__ uint64_t word_sumsq(const uint4 &xv, uint64_t acc) {
 // then every thread adds the 16 warp sums in the same order.  Alternating
 // the buffer between calls keeps a call's writes clear of the previous
 // call's reads (every thread has passed this call's barrier by then).
-__device__ __forceinline__ float block_sum(float v, float (*red)[kNThreads / 32], int &flip) {
+template <int THREADS>
+__device__ __forceinline__ float block_sum(float v, float (*red)[THREADS / 32], int &flip) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -109,20 +112,21 @@ __device__ __forceinline__ float block_sum(float v, float (*red)[kNThreads / 32]
     __syncthreads();
     float t = 0.0f;
 #pragma unroll
-    for (int i = 0; i < kNThreads / 32; ++i) t += red[flip][i];
+    for (int i = 0; i < THREADS / 32; ++i) t += red[flip][i];
     flip ^= 1;
     return t;
 }
 
 // the same for a maximum of magnitude bits
-__device__ __forceinline__ uint32_t block_max(uint32_t v, uint32_t (*red)[kNThreads / 32], int &flip) {
+template <int THREADS>
+__device__ __forceinline__ uint32_t block_max(uint32_t v, uint32_t (*red)[THREADS / 32], int &flip) {
     v = __reduce_max_sync(0xFFFFFFFFu, v);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (lane == 0) red[flip][warp] = v;
     __syncthreads();
     uint32_t t = 0;
 #pragma unroll
-    for (int i = 0; i < kNThreads / 32; ++i) t = max(t, red[flip][i]);
+    for (int i = 0; i < THREADS / 32; ++i) t = max(t, red[flip][i]);
     flip ^= 1;
     return t;
 }
@@ -142,12 +146,13 @@ struct NormArgs {
     unsigned stall;
 };
 
-template <int DT, int NW>
-__global__ void __launch_bounds__(kNThreads, 1) rmsnorm_quant_kernel(const NormArgs a) {
+template <int DT, int THREADS, int NW>
+__global__ void __launch_bounds__(THREADS) rmsnorm_quant_kernel(const NormArgs a) {
+    constexpr int kNThreads = THREADS;
     extern __shared__ __align__(128) uint4 rows_smem[];
     __shared__ __align__(8) uint64_t full[kNormMaxStages];
-    __shared__ float fred[2][kNThreads / 32];
-    __shared__ uint32_t ured[2][kNThreads / 32];
+    __shared__ float fred[2][THREADS / 32];
+    __shared__ uint32_t ured[2][THREADS / 32];
     __shared__ uint32_t bred[33];
     __shared__ int abort_sh;
     __shared__ unsigned epoch_sh;
@@ -227,7 +232,7 @@ __global__ void __launch_bounds__(kNThreads, 1) rmsnorm_quant_kernel(const NormA
         }
         const float part = __fadd_rn(__uint_as_float(static_cast<uint32_t>(acc)),
                                      __uint_as_float(static_cast<uint32_t>(acc >> 32)));
-        const float ss = block_sum(part, fred, fflip);
+        const float ss = block_sum<THREADS>(part, fred, fflip);
         const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(a.K)), a.eps)));
         return f2_pack(__float_as_uint(r), __float_as_uint(r));
     };
@@ -279,7 +284,7 @@ __global__ void __launch_bounds__(kNThreads, 1) rmsnorm_quant_kernel(const NormA
                 }
             }
         } else if (a.mode == kNqPerToken) {
-            const uint32_t rm = block_max(fold_mag<DT>(m), ured, uflip);
+            const uint32_t rm = block_max<THREADS>(fold_mag<DT>(m), ured, uflip);
             const float sc = scale_from_amax(mag_bits_to_float<DT>(rm));
             if (tid == 0) a.scale[row] = sc;
             const Quot d = Quot::make<DT>(sc);
@@ -351,38 +356,51 @@ teardown:
 __global__ void set_one_kernel(float *scale) { *scale = 1.0f; }
 
 constexpr int kMaxDevicesN = 64;
-std::atomic<int> g_norm_ready[kMaxDevicesN][2][4];
+constexpr int kNormVariants = 8;  // (dtype, threads, words per thread) instances
+std::atomic<int> g_norm_ready[kMaxDevicesN][2][kNormVariants];
 
-template <int DT, int NW>
-bool norm_prepare(int dt_idx, int nw_idx) {
+template <int DT, int THREADS, int NW>
+bool norm_prepare(int variant) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesN) return false;
-    if (g_norm_ready[dev][dt_idx][nw_idx].load(std::memory_order_acquire)) return true;
-    if (cudaFuncSetAttribute(rmsnorm_quant_kernel<DT, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kNormSmemBudget) != cudaSuccess)
+    auto &ready = g_norm_ready[dev][DT == FP8L_BF16 ? 1 : 0][variant];
+    if (ready.load(std::memory_order_acquire)) return true;
+    if (cudaFuncSetAttribute(rmsnorm_quant_kernel<DT, THREADS, NW>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kNormSmemBudget) != cudaSuccess)
         return false;
-    g_norm_ready[dev][dt_idx][nw_idx].store(1, std::memory_order_release);
+    ready.store(1, std::memory_order_release);
     return true;
 }
 
-template <int DT, int NW>
-int launch_norm(NormArgs a, int sms, cudaStream_t stream) {
-    if (!norm_prepare<DT, NW>(DT == FP8L_BF16 ? 1 : 0, NW == 1 ? 0 : NW == 2 ? 1 : NW == 4 ? 2 : 3))
-        return FP8L_ECUDA;
-    const int grid = a.M < sms ? a.M : sms;
-    const int rows_per = (a.M + grid - 1) / grid;
+// Blocks per SM and stages: up to 4 blocks of 256 threads (2 of 512) share
+// the SM's row stages; the grid is every block that fits at once (all
+// co-resident, as the dynamic mode's grid barrier needs), at most one per
+// row.
+template <int DT, int THREADS, int NW>
+int launch_norm(NormArgs a, int sms, int variant, cudaStream_t stream) {
+    if (!norm_prepare<DT, THREADS, NW>(variant)) return FP8L_ECUDA;
     const int row_bytes = a.K * 2;
-    int stages = kNormSmemBudget / row_bytes;
-    if (stages > kNormMaxStages) stages = kNormMaxStages;
-    if (stages > rows_per) stages = rows_per;
+    const int want = THREADS == 256 ? 4 : 2;
+    int stages = (kNormSmemBudget / want) / row_bytes;
     if (stages < 1) stages = 1;
+    if (stages > kNormMaxStages) stages = kNormMaxStages;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rmsnorm_quant_kernel<DT, THREADS, NW>,
+                                                      THREADS, static_cast<size_t>(stages) * row_bytes) !=
+            cudaSuccess ||
+        per_sm < 1)
+        return FP8L_ECUDA;
+    const int64_t slots = int64_t(per_sm) * sms;
+    const int grid = static_cast<int>(a.M < slots ? a.M : slots);
+    const int rows_per = (a.M + grid - 1) / grid;
+    if (stages > rows_per) stages = rows_per;
     a.stages = stages;
     const WaitConfig wc = wait_config();
     a.wait_cycles = wc.cycles;
     a.stall = wc.stall;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(kNThreads, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(stages) * row_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -390,17 +408,19 @@ int launch_norm(NormArgs a, int sms, cudaStream_t stream) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = a.mode == kNqDynamic ? 1 : 0;
-    if (cudaLaunchKernelEx(&cfg, rmsnorm_quant_kernel<DT, NW>, a) != cudaSuccess) return FP8L_ECUDA;
+    if (cudaLaunchKernelEx(&cfg, rmsnorm_quant_kernel<DT, THREADS, NW>, a) != cudaSuccess)
+        return FP8L_ECUDA;
     return launch_status();
 }
 
 template <int DT>
 int dispatch_nw(const NormArgs &a, int sms, cudaStream_t stream) {
-    const int words_per_thread = (a.K / 8 + kNThreads - 1) / kNThreads;
-    if (words_per_thread <= 1) return launch_norm<DT, 1>(a, sms, stream);
-    if (words_per_thread <= 2) return launch_norm<DT, 2>(a, sms, stream);
-    if (words_per_thread <= 4) return launch_norm<DT, 4>(a, sms, stream);
-    return launch_norm<DT, 8>(a, sms, stream);
+    const int words = a.K / 8;
+    if (words <= 256) return launch_norm<DT, 256, 1>(a, sms, 0, stream);
+    if (words <= 512) return launch_norm<DT, 256, 2>(a, sms, 1, stream);
+    if (words <= 1024) return launch_norm<DT, 256, 4>(a, sms, 2, stream);
+    if (words <= 2048) return launch_norm<DT, 512, 4>(a, sms, 3, stream);
+    return launch_norm<DT, 512, 8>(a, sms, 4, stream);
 }
 
 }  // namespace

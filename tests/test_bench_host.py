@@ -72,8 +72,9 @@ def _fake_tree(root, skinny_src):
 
 
 def test_traffic_lookup_follows_the_kernel_source(tmp_path, monkeypatch):
+    # the hash covers the kernel's file and the library headers it includes
     root = str(tmp_path)
-    _fake_tree(root, "// kernel v1\n")
+    _fake_tree(root, '#include "common.cuh"\n// kernel v1\n')
     monkeypatch.setattr(bench, "ROOT", root)
     h = bench.kernel_source_hash("skinny.cu")
     with open(os.path.join(root, "profiles", "traffic.md"), "w") as f:
@@ -89,7 +90,7 @@ def test_traffic_lookup_follows_the_kernel_source(tmp_path, monkeypatch):
         f.write("// edited\n")
     assert bench.traffic_from_profile("w8a16_skinny") is None
     with open(os.path.join(root, "fp8_quantized_linear_gb300", "csrc", "skinny.cu"), "w") as f:
-        f.write("// kernel v1\n")
+        f.write('#include "common.cuh"\n// kernel v1\n')
     assert bench.traffic_from_profile("w8a16_skinny") is not None
     with open(os.path.join(root, "fp8_quantized_linear_gb300", "csrc", "common.cuh"), "a") as f:
         f.write("// edited\n")
