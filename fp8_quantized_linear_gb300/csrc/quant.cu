@@ -421,21 +421,8 @@ struct TmaPlan {
     int64_t total_pieces;
 };
 
-// Tensors up to this size run as one block: a decode step's activations are
-// a few kilobytes, and one block streaming them through its stages ends
-// sooner than many blocks that then meet at a grid barrier.
-constexpr int64_t kSingleBlockBytes = 128 * 1024;
-
 TmaPlan plan_tma(int64_t n_words, int sms, int64_t l2_bytes) {
     TmaPlan p;
-    if (n_words * 16 <= kSingleBlockBytes) {
-        p.piece_words = kPieceWords;
-        p.total_pieces = (n_words + kPieceWords - 1) / kPieceWords;  // 0 for a tail-only tensor
-        p.grid = 1;
-        p.stages = static_cast<int>(p.total_pieces < 1 ? 1 : (p.total_pieces < kStages ? p.total_pieces : kStages));
-        p.keep_pieces = 0;
-        return p;
-    }
     const int64_t per_block = (n_words + int64_t(sms) * kPieceWords - 1) / (int64_t(sms) * kPieceWords);
     int64_t pw = per_block > 0 ? (n_words + int64_t(sms) * per_block - 1) / (int64_t(sms) * per_block) : 1;
     pw = (pw + 63) / 64 * 64;  // whole kilobytes
