@@ -66,6 +66,9 @@ METRIC = "FP8 scaled-GEMM TFLOP/s (GB/s at M<=16) and % of GB300 roofline"
 HEADLINE = "llama70b_static_fp8out"
 ENTRY_WORKLOADS = ("decode_w8a16", "prefill_w8a8_outliers", "llama3_8b_w8a8_sweep", "tiny_w8a8")
 HBM_TARGET = 0.70  # fraction of HBM bandwidth the M <= 16 shapes aim for
+# bench names of the three W8A8 kernels fp8_scaled_mm may run
+W8A8_KINDS = {"stream": "scaled_mm_skinny", "swapped": "scaled_mm_swapped",
+              "tiled": "scaled_mm_tcgen05"}
 L2_BYTES = 126 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -384,16 +387,17 @@ class Workload:
                             lambda it=it, dyn=dynamic: fl.fp8_quant_per_tensor(
                                 it["x"], q=it["qa"], scale=it["sa"], dynamic=dyn, ws=ws),
                             3 * M * K, "bytes", 1, (M, N, K)))
-            kind = "scaled_mm_skinny" if M <= 16 else "scaled_mm_tcgen05"
+            kind = W8A8_KINDS[fl.scaled_mm_kernel(M, N, K)]
+            streams = kind != "scaled_mm_tcgen05"  # bound by reading the weights
             units = (w8a8_bytes(M, N, K, it["y"].element_size(), wl.w_scale == "channel")
-                     if M <= 16 else 2 * M * N * K)
+                     if streams else 2 * M * N * K)
             out.append(Call(kind,
                             lambda it=it: fl.fp8_scaled_mm(it["qa"], it["qw"], it["sa"], it["sw"],
                                                            out_dtype=it["y"].dtype,
                                                            out_scale=it.get("os"), y=it["y"],
                                                            ws=ws, stable_weights=True,
                                                            single_sm=Workload.single_sm),
-                            units, "bytes" if M <= 16 else "flops", 1, (M, N, K)))
+                            units, "bytes" if streams else "flops", 1, (M, N, K)))
         return out
 
     def step_units(self):
@@ -679,6 +683,7 @@ def roofline(per_kind, peaks, ms_per_step, sustained=False):
 
 
 KERNEL_SOURCES = {"w8a16_skinny": "skinny.cu", "scaled_mm_skinny": "skinny.cu",
+                  "scaled_mm_swapped": "gemm_swapab.cu",
                   "scaled_mm_tcgen05": "gemm_tcgen05.cu", "quant_dynamic": "quant.cu",
                   "quant_static": "quant.cu"}
 
@@ -1043,7 +1048,7 @@ def per_shape(work, peaks, steps):
             kind = "w8a16_skinny"
         else:
             nbytes = w8a8_bytes(M, N, K, base["y"].element_size(), wl.w_scale == "channel")
-            peak, kind = fp8_peak, "scaled_mm_skinny" if M <= 16 else "scaled_mm_tcgen05"
+            peak, kind = fp8_peak, W8A8_KINDS[fl.scaled_mm_kernel(M, N, K)]
         n_rot = max(1, min(64, math.ceil(3 * L2_BYTES / nbytes)))
         copies = [base] + [{k: (v.clone() if isinstance(v, torch.Tensor) else v)
                             for k, v in base.items()} for _ in range(n_rot - 1)]

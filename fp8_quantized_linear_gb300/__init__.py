@@ -7,7 +7,9 @@ carry the C entry points' names:
   fp8_quant_per_tensor  dynamic or static per-tensor quantization to E4M3
   fp8_quant_per_row     per-row quantization (weights at setup; per-token activations)
   fp8_rmsnorm_quant     RMSNorm with the activation quantization fused into it
-  fp8_scaled_mm         W8A8 scaled product (tcgen05 GEMM; M <= 16 streams W)
+  fp8_scaled_mm         W8A8 scaled product (tcgen05 products; few tokens and
+                        small weights streamed on the CUDA cores)
+  scaled_mm_kernel      which of the three kernels fp8_scaled_mm runs for a shape
   fp8_grouped_mm        W8A8 products of mixture-of-experts layers (device offsets)
   fp8_w8a16_mm          weight-only fp16/bf16 x E4M3 product
   fp8_pack_w8a16_weights  weights permuted once into the order that product
@@ -18,4 +20,5 @@ The library is loaded on first use; nothing here computes on the CPU.
 from ._binding import (  # noqa: F401
     BF16, E4M3, F16, F32, Fp8LinearError, LIB_PATH, fp8_grouped_mm, fp8_pack_w8a16_weights,
     fp8_packed_weight_bytes, fp8_quant_per_row, fp8_quant_per_tensor, fp8_scaled_mm,
-    fp8_rmsnorm_quant, fp8_w8a16_mm, fp8l_debug_waits, fp8l_read_status, fp8l_workspace_bytes, load, strerror, workspace)
+    fp8_rmsnorm_quant, fp8_w8a16_mm, fp8l_debug_waits, fp8l_read_status, fp8l_workspace_bytes, load,
+    scaled_mm_kernel, strerror, workspace)

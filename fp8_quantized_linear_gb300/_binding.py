@@ -17,12 +17,13 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfp8linear.so")
 
-ABI_VERSION = 3  # the library version this binding is written for
+ABI_VERSION = 4  # the library version this binding is written for
 F16, BF16, E4M3, F32 = 0, 1, 2, 3
 WEIGHTS_STABLE = 1
 WEIGHTS_PACKED = 2
 A_PER_TOKEN = 4
 SINGLE_SM_TILES = 8
+KERNELS = {"auto": 0, "stream": 16, "swapped": 32, "tiled": 48}  # FP8L_KERNEL_*
 OK, EINVAL, ESHAPE, EALIGN, ECUDA, ETIMEOUT, EUNSUPPORTED = range(7)
 
 _DTYPE_CODE = {torch.float16: F16, torch.bfloat16: BF16, torch.float32: F32,
@@ -73,6 +74,8 @@ def load():
         lib.fp8_quant_per_row.argtypes = [P, I, I64, I64, P, P, P]
         lib.fp8_scaled_mm.restype = I
         lib.fp8_scaled_mm.argtypes = [P, P, I64, I64, I64, P, P, I, P, P, I, P, ctypes.c_uint, P]
+        lib.fp8_scaled_mm_kernel.restype = ctypes.c_uint
+        lib.fp8_scaled_mm_kernel.argtypes = [I64, I64, I64, ctypes.c_uint]
         lib.fp8_w8a16_mm.restype = I
         lib.fp8_w8a16_mm.argtypes = [P, I, P, P, I64, I64, I64, P, ctypes.c_uint, P]
         lib.fp8_packed_weight_bytes.restype = ctypes.c_size_t
@@ -229,17 +232,26 @@ def fp8_quant_per_row(x: torch.Tensor, q: torch.Tensor | None = None,
     return q, row_scale
 
 
+def scaled_mm_kernel(M: int, N: int, K: int, kernel: str = "auto") -> str:
+    """Name ("stream", "swapped" or "tiled") of the kernel fp8_scaled_mm runs
+    for this shape and kernel choice (fp8_scaled_mm_kernel; no GPU needed)."""
+    code = load().fp8_scaled_mm_kernel(M, N, K, KERNELS[kernel])
+    return {v: k for k, v in KERNELS.items()}[code]
+
+
 def fp8_scaled_mm(a: torch.Tensor, w: torch.Tensor, a_scale: torch.Tensor,
                   w_scale: torch.Tensor, out_dtype=torch.bfloat16,
                   out_scale: torch.Tensor | None = None, y: torch.Tensor | None = None,
                   ws: torch.Tensor | None = None, stable_weights: bool = False,
-                  per_token: bool | None = None, single_sm: bool = False) -> torch.Tensor:
+                  per_token: bool | None = None, single_sm: bool = False,
+                  kernel: str = "auto") -> torch.Tensor:
     """W8A8 product of E4M3 a [M, K] and w [N, K] with a per-tensor ([1]) or
     per-token ([M]) a_scale and a per-tensor ([1]) or per-channel ([N])
     w_scale.  out_dtype bf16 / fp16, or uint8 (E4M3 codes, needs out_scale).
     stable_weights sets FP8L_WEIGHTS_STABLE (no work in flight on the stream
     writes w or w_scale); per_token (default: a_scale has M > 1 entries) sets
-    FP8L_A_PER_TOKEN; single_sm sets FP8L_SINGLE_SM_TILES."""
+    FP8L_A_PER_TOKEN; single_sm sets FP8L_SINGLE_SM_TILES; kernel ("auto",
+    "stream", "swapped" or "tiled") sets the FP8L_KERNEL_* choice."""
     _need_cuda(a, w, a_scale, w_scale, out_scale, y, ws)
     a, w = _codes(a), _codes(w)
     M, K = a.shape
@@ -261,7 +273,7 @@ def fp8_scaled_mm(a: torch.Tensor, w: torch.Tensor, a_scale: torch.Tensor,
     if a_scale.numel() != (M if per_token else 1):
         raise ValueError("a_scale must have 1 entry, or M with per_token")
     flags = ((WEIGHTS_STABLE if stable_weights else 0) | (A_PER_TOKEN if per_token else 0) |
-             (SINGLE_SM_TILES if single_sm else 0))
+             (SINGLE_SM_TILES if single_sm else 0) | KERNELS[kernel])
     with torch.cuda.device(a.device):
         st = load().fp8_scaled_mm(
             a.data_ptr(), w.data_ptr(), M, N, K, a_scale.data_ptr(), w_scale.data_ptr(),

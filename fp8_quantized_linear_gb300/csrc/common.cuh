@@ -101,6 +101,10 @@ int launch_skinny_e4m3(const uint8_t *a, const uint8_t *w, int M, int N, int K,
                        const float *a_scale, int a_per_token, const float *w_scale,
                        int w_per_channel, const float *out_scale, void *y, int out_dtype,
                        bool stable_weights, cudaStream_t stream);
+int launch_swapab(const uint8_t *a, const uint8_t *w, int M, int N, int K, const float *a_scale,
+                  int a_per_token, const float *w_scale, int w_per_channel,
+                  const float *out_scale, void *y, int out_dtype, unsigned *status, int sms,
+                  bool stable, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // device helpers

@@ -34,7 +34,7 @@
 
 #include <atomic>
 
-#include "common.cuh"
+#include "tc_device.cuh"
 
 namespace fp8l {
 namespace {
@@ -77,119 +77,6 @@ struct GemmParams {
     int split;  // > 1: a cluster of `split` CTAs shares one tile and splits its k-blocks
 };
 
-// ---------------------------------------------------------------- PTX wrappers
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-// Bounded wait for the phase of parity `parity`.  Gives up when another
-// role raised the abort flag, or after `limit` cycles (then raises it and
-// records the time-out).
-// In a CTA pair (peer_abort != 0, the peer's flag as a shared::cluster
-// address) a time-out raises the peer's flag too, and the wait acquires at
-// cluster scope (the barrier may be completed by the peer CTA).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                       unsigned *status, long long limit, uint32_t peer_abort = 0) {
-    auto ready = [&]() { return peer_abort ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
-    if (ready()) return true;
-    const long long t0 = clock64();
-    for (uint32_t i = 1;; ++i) {
-        if (ready()) return true;
-        if ((i & 63u) == 0u) {
-            if (*abort_flag) return false;
-            if (clock64() - t0 > limit) {
-                *abort_flag = 1;
-                if (peer_abort)
-                    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_abort), "r"(1) : "memory");
-                atomicOr(status, kStatusTimeout);
-                return false;
-            }
-        }
-    }
-}
-
-// The common case first: one test of the phase inline, the bounded loop only
-// when it is not complete yet (keeps the MMA issue loop short).
-__device__ __forceinline__ bool mbar_wait_fast(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                               unsigned *status, long long limit,
-                                               uint32_t peer_abort = 0) {
-    if (peer_abort ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-    return mbar_wait(bar, parity, abort_flag, status, limit, peer_abort);
-}
-
-// Bounded wait used while tearing down: ignores the abort flag.
-__device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, unsigned *status) {
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > kDefaultWaitCycles) {
-            atomicOr(status, kStatusTimeout);
-            return false;
-        }
-    }
-    return true;
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor (tcgen05 format) of a K-major operand tile
-// laid out by TMA with the 128-byte swizzle: 128-byte rows, 8-row groups
-// 1024 bytes apart (stride byte offset), version field 1, swizzle mode 2.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
-           (static_cast<uint64_t>(1) << 16) |
-           (static_cast<uint64_t>(1024 >> 4) << 32) |
-           (static_cast<uint64_t>(1) << 46) |
-           (static_cast<uint64_t>(2) << 61);
-}
-
 // Instruction descriptor, kind::f8f6f4: D f32 (bits 4-5 = 1), A and B E4M3
 // (format 0, bits 7-9 and 10-12), both K-major (bits 15, 16 = 0),
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
@@ -204,83 +91,6 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t
         "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
         : "memory");
 }
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-}
-
-// shared::cluster address of `local` (a shared::cta address) in CTA `rank`
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// ---------------------------------------------------------------- epilogue
-
-__device__ __forceinline__ uint32_t pack_out16(float a, float b, int out_dtype) {
-    if (out_dtype == FP8L_BF16) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-        return *reinterpret_cast<uint32_t *>(&h);
-    }
-    __half2 h = __floats2half2_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-
-__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
-    return static_cast<uint32_t>(
-        __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
-}
-
-// E4M3 output codes of v / output_scale.  The quotient is the correctly
-// rounded RN(v / os) without a division: with y = RN(1/os), q0 = RN(v y) and
-// two corrections q <- RN(q + RN(v - os q) y) (fused multiply-adds), the
-// second of which is correctly rounded by Markstein's theorem (P. Markstein,
-// IBM J. Res. Develop. 34(1), 1990) when the residual does not underflow and
-// nothing overflows.  That holds for 2^-92 <= os <= 2^100 once |v| is
-// clamped to 1024 os (every code from 464 os up saturates to 448 anyway);
-// other output scales take the IEEE division.
-struct OutDiv {
-    float os, y, cap;
-    bool fast;
-    __device__ __forceinline__ static OutDiv make(float os) {
-        OutDiv d;
-        d.os = os;
-        d.y = __frcp_rn(os);
-        d.cap = 1024.0f * os;
-        d.fast = os >= 0x1p-92f && os <= 0x1p100f;
-        return d;
-    }
-    __device__ __forceinline__ float quot(float v) const {
-        if (!fast) return __fdiv_rn(v, os);
-        const float vc = copysignf(fminf(fabsf(v), cap), v);
-        float q = __fmul_rn(vc, y);
-        q = __fmaf_rn(__fmaf_rn(-os, q, vc), y, q);
-        return __fmaf_rn(__fmaf_rn(-os, q, vc), y, q);
-    }
-};
 
 // Scales and stores 32 accumulator columns [n0, n0+32) of row m; sa is the
 // row's activation scale, sa_sw = sa * (per-tensor weight scale) and wsc the
@@ -376,24 +186,6 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, const GroupTa
 constexpr int kPartPitch = BN + 4;  // floats per partial-tile row (conflict-free v4 stores)
 constexpr int kMaxSplit = 4;  // clusters of 8 at this shared-memory size ran 1.4-1.7x slower
 static_assert(BM * kPartPitch * 4 <= STAGES * kStageBytes, "partial tile fits in the ring");
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
-}
-
-// v4 load from CTA `rank`'s shared memory at this CTA's offset `local_addr`
-__device__ __forceinline__ float4 ld_cluster_v4(uint32_t local_addr, uint32_t rank) {
-    const uint32_t remote = map_to_rank(local_addr, rank);
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(remote)
-                 : "memory");
-    return v;
-}
 
 __device__ void split_reduce_store(const GemmParams &p, int tile, int rank, uint32_t sbase) {
     const int mb = tile % p.num_m_blocks;
@@ -717,12 +509,6 @@ constexpr size_t kPSmemBytes = 1024 + size_t(P_STAGES) * kPStageBytes + kPNumBar
 // kind::f8f6f4, D f32, A and B E4M3 K-major, N = 256, M = 256 (pair)
 constexpr uint32_t kIdescPair = (1u << 4) | (uint32_t(P_BN >> 3) << 17) | (uint32_t(256 >> 4) << 24);
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
 // TMA load into this CTA's shared memory, completing on an mbarrier of
 // either CTA of the pair (bar: shared::cluster address)
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int x, int y,
@@ -752,11 +538,6 @@ __device__ __forceinline__ void commit_pair(uint32_t bar) {
         " [%0], %1;" ::"r"(bar),
         "h"(static_cast<uint16_t>(3))
         : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
-                 : "memory");
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -1072,6 +853,38 @@ int launch_tcgen05(const uint8_t *a, const uint8_t *w, int M, int N, int K, cons
 }  // namespace
 }  // namespace fp8l
 
+namespace fp8l {
+namespace {
+
+// The kernel fp8_scaled_mm runs for FP8L_KERNEL_AUTO (per-shape times of the
+// three kernels on GB300, each product alone over rotating operand copies):
+//   - weight streaming on the CUDA cores for few tokens and small weights
+//     (16 MiB at up to 16 tokens, 24 MiB at up to 4), where its shorter
+//     start-up wins (4096 x 4096: 4.9 us against 6.4 us at M = 1);
+//   - the swapped-operand tcgen05 product up to 128 tokens (M = 16 at
+//     28672 x 4096: 21.5 us against 31.6 us streamed on the CUDA cores and
+//     31.8 us on token x channel tiles), except above 64 tokens with 256 MiB
+//     or more of weights, where the token x channel tiles read the
+//     activations from L2 half as often (M = 128, 57344 x 8192: 87.7 us
+//     against 93.1 us);
+//   - token x channel tiles otherwise.
+unsigned choose_kernel(int64_t M, int64_t N, int64_t K) {
+    const int64_t wbytes = N * K;
+    if ((M <= 4 && wbytes <= (int64_t(24) << 20)) || (M <= 16 && wbytes <= (int64_t(16) << 20)))
+        return FP8L_KERNEL_STREAM;
+    if (M <= 128 && !(M > 64 && wbytes >= (int64_t(256) << 20))) return FP8L_KERNEL_SWAPPED;
+    return FP8L_KERNEL_TILED;
+}
+
+}  // namespace
+}  // namespace fp8l
+
+extern "C" unsigned fp8_scaled_mm_kernel(int64_t M, int64_t N, int64_t K, unsigned flags) {
+    const unsigned k = flags & FP8L_KERNEL_MASK;
+    if (k != FP8L_KERNEL_AUTO) return k;
+    return fp8l::choose_kernel(M, N, K);
+}
+
 extern "C" int fp8_scaled_mm(const uint8_t *a, const uint8_t *w, int64_t M, int64_t N, int64_t K,
                              const float *a_scale, const float *w_scale, int w_per_channel,
                              const float *out_scale, void *y, int out_dtype, void *workspace,
@@ -1079,8 +892,10 @@ extern "C" int fp8_scaled_mm(const uint8_t *a, const uint8_t *w, int64_t M, int6
     using namespace fp8l;
     if (out_dtype != FP8L_F16 && out_dtype != FP8L_BF16 && out_dtype != FP8L_E4M3)
         return FP8L_EINVAL;
-    if ((flags & ~(FP8L_WEIGHTS_STABLE | FP8L_A_PER_TOKEN | FP8L_SINGLE_SM_TILES)) != 0u)
+    if ((flags & ~(FP8L_WEIGHTS_STABLE | FP8L_A_PER_TOKEN | FP8L_SINGLE_SM_TILES | FP8L_KERNEL_MASK)) != 0u)
         return FP8L_EINVAL;
+    unsigned kernel = flags & FP8L_KERNEL_MASK;
+    if (kernel == FP8L_KERNEL_SWAPPED && M > 128) return FP8L_ESHAPE;
     if (a_scale == nullptr || w_scale == nullptr || workspace == nullptr || w == nullptr)
         return FP8L_EINVAL;
     if (out_dtype == FP8L_E4M3 && out_scale == nullptr) return FP8L_EINVAL;
@@ -1100,15 +915,20 @@ extern "C" int fp8_scaled_mm(const uint8_t *a, const uint8_t *w, int64_t M, int6
     cudaStream_t s = as_stream(stream);
     const int pc = w_per_channel ? 1 : 0;
     const int pt = (flags & FP8L_A_PER_TOKEN) != 0u ? 1 : 0;
-    if (M <= 16)
+    const bool stable = (flags & FP8L_WEIGHTS_STABLE) != 0u;
+    if (kernel == FP8L_KERNEL_AUTO) kernel = choose_kernel(M, N, K);
+    if (kernel == FP8L_KERNEL_STREAM)
         return launch_skinny_e4m3(a, w, static_cast<int>(M), static_cast<int>(N),
                                   static_cast<int>(K), a_scale, pt, w_scale, pc, out_scale, y,
-                                  out_dtype, (flags & FP8L_WEIGHTS_STABLE) != 0u, s);
+                                  out_dtype, stable, s);
+    if (kernel == FP8L_KERNEL_SWAPPED)
+        return launch_swapab(a, w, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                             a_scale, pt, w_scale, pc, out_scale, y, out_dtype,
+                             status_word(workspace), sms, stable, s);
     return launch_tcgen05(a, w, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
                           a_scale, pt, w_scale, pc, out_scale, y, out_dtype,
                           status_word(workspace), sms, s, nullptr, 0,
-                          (flags & FP8L_SINGLE_SM_TILES) != 0u,
-                          (flags & FP8L_WEIGHTS_STABLE) != 0u);
+                          (flags & FP8L_SINGLE_SM_TILES) != 0u, stable);
 }
 
 extern "C" int fp8_grouped_mm(const uint8_t *a, const uint8_t *w, const int32_t *group_offsets,

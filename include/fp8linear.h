@@ -51,7 +51,7 @@ extern "C" {
  * 3 adds fp8l_debug_waits, the per-token activation scales
  * (FP8L_A_PER_TOKEN), fp8_rmsnorm_quant and fp8_grouped_mm.  Each change is additive: a caller written for an
  * earlier version runs unchanged. */
-#define FP8L_ABI_VERSION 3
+#define FP8L_ABI_VERSION 4
 
 /* Only the entry points below are exported from the shared library. */
 #if defined(__GNUC__)
@@ -100,6 +100,21 @@ enum fp8l_status {
  * fp32 over k in the same blocks, and their results agree within the
  * layer's tolerance). */
 #define FP8L_SINGLE_SM_TILES 8u
+
+/* Kernel choice of fp8_scaled_mm (a tuning and testing option; every
+ * kernel accumulates in fp32 and their results agree within the layer's
+ * tolerance).  FP8L_KERNEL_AUTO (0) picks by M as fp8_scaled_mm describes.
+ *   FP8L_KERNEL_STREAM   weight streaming on the CUDA cores (mma.sync),
+ *                        any M, in groups of 16 rows;
+ *   FP8L_KERNEL_SWAPPED  tcgen05 product with the operands swapped (128
+ *                        weight rows by M tokens per tile), 1 <= M <= 128
+ *                        (FP8L_ESHAPE otherwise);
+ *   FP8L_KERNEL_TILED    tcgen05 product on token x channel tiles, any M. */
+#define FP8L_KERNEL_AUTO 0u
+#define FP8L_KERNEL_STREAM 16u
+#define FP8L_KERNEL_SWAPPED 32u
+#define FP8L_KERNEL_TILED 48u
+#define FP8L_KERNEL_MASK 48u
 
 /* Element types. */
 enum fp8l_dtype {
@@ -178,17 +193,28 @@ FP8L_API int fp8_quant_per_row(const void *x, int x_dtype, int64_t rows, int64_t
  * when out_dtype is FP8L_E4M3 and ignored otherwise.
  * M >= 0 (M == 0 launches nothing); N and K are positive multiples of 16
  * (the FP8 GEMM shape rule), N, K <= 2^20, M <= 2^31 - 1.
- * M <= 16 runs a weight-streaming kernel; larger M runs a tcgen05 tensor
- * core kernel: clusters of CTAs splitting K when the tiles are few, else a
- * persistent kernel whose 256 x 256 tiles each span a pair of SMs
- * (tcgen05.mma.cta_group::2), or 128 x 256 tiles on one SM each with
- * FP8L_SINGLE_SM_TILES.  workspace: fp8l_workspace_bytes() bytes (status word).
- * flags: any of FP8L_WEIGHTS_STABLE, FP8L_A_PER_TOKEN and
- * FP8L_SINGLE_SM_TILES (other bits are FP8L_EINVAL). */
+ * Kernels (fp8_scaled_mm_kernel names the one a call runs): up to 16 tokens
+ * with small weights, weight streaming on the CUDA cores; up to 128 tokens,
+ * a tcgen05 product with the operands swapped (128 weight rows by the
+ * tokens per tile, clusters of CTAs splitting K when the weight blocks are
+ * few); otherwise tcgen05 token x channel tiles: a persistent kernel whose
+ * 256 x 256 tiles each span a pair of SMs (tcgen05.mma.cta_group::2), or
+ * 128 x 256 tiles on one SM each with FP8L_SINGLE_SM_TILES, or clusters
+ * splitting K when the tiles are few.  workspace: fp8l_workspace_bytes()
+ * bytes (status word).  flags: any of FP8L_WEIGHTS_STABLE,
+ * FP8L_A_PER_TOKEN, FP8L_SINGLE_SM_TILES and one FP8L_KERNEL_* choice
+ * (other bits are FP8L_EINVAL; FP8L_KERNEL_SWAPPED with M > 128 is
+ * FP8L_ESHAPE). */
 FP8L_API int fp8_scaled_mm(const uint8_t *a, const uint8_t *w, int64_t M, int64_t N,
                   int64_t K, const float *a_scale, const float *w_scale,
                   int w_per_channel, const float *out_scale, void *y,
                   int out_dtype, void *workspace, unsigned flags, void *stream);
+
+/* The kernel fp8_scaled_mm runs for this shape and these flags:
+ * FP8L_KERNEL_STREAM, FP8L_KERNEL_SWAPPED or FP8L_KERNEL_TILED (the flags'
+ * own choice when they make one).  A pure function of its arguments; needs
+ * no GPU. */
+FP8L_API unsigned fp8_scaled_mm_kernel(int64_t M, int64_t N, int64_t K, unsigned flags);
 
 /* W8A16 weight-only product ("Marlin fp8"): 16-bit activations times E4M3
  * weights with one scale per output channel.

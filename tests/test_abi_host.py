@@ -54,7 +54,7 @@ def test_only_c_abi_symbols_exported(lib):
 
 def test_constants(lib):
     import fp8_quantized_linear_gb300 as fl
-    assert lib.fp8l_abi_version() == fl._binding.ABI_VERSION == 3
+    assert lib.fp8l_abi_version() == fl._binding.ABI_VERSION == 4
     assert fl.fp8l_workspace_bytes() >= 4096 and fl.fp8l_workspace_bytes() % 16 == 0
     for code in range(7):
         assert fl.strerror(code)
@@ -91,6 +91,28 @@ def test_scaled_mm_argument_errors(lib):
     assert call(y=A16 + 4) == b.EALIGN
     assert call(sw=A16 + 2) == b.EALIGN
     assert call(fl=2) == b.EINVAL
+    assert call(fl=64) == b.EINVAL
+    assert call(fl=b.KERNELS["swapped"], M=129) == b.ESHAPE
+
+
+def test_scaled_mm_kernel_choice(lib):
+    # which kernel fp8_scaled_mm runs: a pure function of the shape, no GPU
+    import fp8_quantized_linear_gb300 as fl
+    k = fl.scaled_mm_kernel
+    assert k(16, 256, 512) == "stream"        # tiny layer
+    assert k(1, 4096, 4096) == "stream"       # 16 MiB of weights
+    assert k(16, 4096, 4096) == "stream"
+    assert k(4, 6144, 4096) == "stream"       # 24 MiB at up to 4 tokens
+    assert k(16, 6144, 4096) == "swapped"
+    assert k(1, 28672, 4096) == "swapped"
+    assert k(64, 10240, 8192) == "swapped"
+    assert k(128, 4096, 14336) == "swapped"
+    assert k(128, 57344, 8192) == "tiled"     # 448 MiB above 64 tokens
+    assert k(64, 57344, 8192) == "swapped"
+    assert k(129, 4096, 4096) == "tiled"
+    assert k(1024, 4096, 4096) == "tiled"
+    for name in ("stream", "swapped", "tiled"):  # an explicit choice is kept
+        assert k(1024, 4096, 4096, name) == name
 
 
 def test_w8a16_argument_errors(lib):

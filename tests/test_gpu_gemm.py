@@ -33,16 +33,18 @@ def _operands(M, N, K, per_channel, seed, outliers=0.0):
 @pytest.mark.parametrize("M,N,K", [(17, 16, 16), (32, 48, 80), (128, 256, 128), (129, 272, 144),
                                    (200, 512, 512), (300, 784, 1040), (512, 1024, 4096)])
 def test_tcgen05_small_shapes(M, N, K, per_channel, out):
+    # token x channel tiles at every M (the automatic choice runs the
+    # swapped-operand product up to 128 tokens)
     _, _, qa, sa, qw, sw = _operands(M, N, K, per_channel, seed=M * 7 + N * 3 + K)
     y_ref = oracle.scaled_mm_ref(qa, qw, sa, sw)
     if out == "e4m3":
         os_ = np.float32(np.abs(y_ref).max() / 448.0 * 0.8)
         y = fl.fp8_scaled_mm(dev(qa), dev(qw), scalar(sa), dev(sw), out_dtype=torch.uint8,
-                             out_scale=scalar(os_))
+                             out_scale=scalar(os_), kernel="tiled")
         assert_e4m3_close(host(y), y_ref, os_, (M, N, K))
     else:
         dt = torch.bfloat16 if out == "bf16" else torch.float16
-        y = fl.fp8_scaled_mm(dev(qa), dev(qw), scalar(sa), dev(sw), out_dtype=dt)
+        y = fl.fp8_scaled_mm(dev(qa), dev(qw), scalar(sa), dev(sw), out_dtype=dt, kernel="tiled")
         assert_gemm_close(host(y), y_ref, (M, N, K, out))
     assert_status_ok()
 
@@ -203,7 +205,8 @@ def test_tcgen05_split_k_exact_integer(M, N, K):
     qa = codes[rng.integers(0, 7, (M, K))]
     qw = codes[rng.integers(0, 7, (N, K))]
     sw = np.array([2.0 ** (n % 5 - 2) for n in range(N)], np.float32)
-    y = host(fl.fp8_scaled_mm(dev(qa), dev(qw), scalar(0.5), dev(sw), out_dtype=torch.bfloat16))
+    y = host(fl.fp8_scaled_mm(dev(qa), dev(qw), scalar(0.5), dev(sw), out_dtype=torch.bfloat16,
+                              kernel="tiled"))
     exact = oracle.scaled_mm_ref(qa, qw, np.float32(0.5), sw)
     want = torch.from_numpy(exact).to(torch.bfloat16).float().numpy()
     assert np.array_equal(y, want)

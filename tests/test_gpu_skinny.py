@@ -99,7 +99,7 @@ def test_w8a16_empty_batch():
     assert y.shape == (0, 32)
 
 
-def _w8a8_small(M, N, K, per_channel, out, seed):
+def _w8a8_small(M, N, K, per_channel, out, seed, kernel):
     x = synthetic.activation(M, K, torch.bfloat16, seed=seed)
     w = synthetic.weight(N, K, torch.bfloat16, seed=seed)
     qa, sa = oracle.quant_per_tensor(x)
@@ -112,20 +112,23 @@ def _w8a8_small(M, N, K, per_channel, out, seed):
     if out == "e4m3":
         os_ = np.float32(np.abs(y_ref).max() / 448.0 * 0.75)  # a few outputs saturate
         y = fl.fp8_scaled_mm(dev(qa), dev(qw), scalar(sa), dev(sw), out_dtype=torch.uint8,
-                             out_scale=scalar(os_))
+                             out_scale=scalar(os_), kernel=kernel)
         assert_e4m3_close(host(y), y_ref, os_, (M, N, K))
     else:
         dt = torch.bfloat16 if out == "bf16" else torch.float16
-        y = fl.fp8_scaled_mm(dev(qa), dev(qw), scalar(sa), dev(sw), out_dtype=dt)
+        y = fl.fp8_scaled_mm(dev(qa), dev(qw), scalar(sa), dev(sw), out_dtype=dt, kernel=kernel)
         assert_gemm_close(host(y), y_ref, (M, N, K, out))
 
 
+# the CUDA-core weight-streaming kernel, and the swapped-operand tcgen05
+# product the automatic choice takes for most of these shapes
+@pytest.mark.parametrize("kernel", ["stream", "swapped"])
 @pytest.mark.parametrize("out", ["bf16", "fp16", "e4m3"])
 @pytest.mark.parametrize("per_channel", [False, True])
 @pytest.mark.parametrize("M,N,K", [(1, 16, 16), (1, 256, 512), (5, 48, 80), (16, 256, 512),
                                    (16, 4096, 4096), (1, 28672, 4096), (16, 4096, 14336)])
-def test_w8a8_small_m(M, N, K, per_channel, out):
-    _w8a8_small(M, N, K, per_channel, out, seed=M + N + K)
+def test_w8a8_small_m(M, N, K, per_channel, out, kernel):
+    _w8a8_small(M, N, K, per_channel, out, seed=M + N + K, kernel=kernel)
 
 
 @pytest.mark.parametrize("M,K", [(16, 1024), (8, 1024), (3, 4096), (8, 1040)])
@@ -140,7 +143,8 @@ def test_w8a8_small_m_exact_integer(M, K):
     qa = codes[rng.integers(0, 7, (M, K))]
     qw = codes[rng.integers(0, 7, (N, K))]
     sw = np.array([2.0 ** -(n % 4) for n in range(N)], np.float32)
-    y = host(fl.fp8_scaled_mm(dev(qa), dev(qw), scalar(0.5), dev(sw), out_dtype=torch.bfloat16))
+    y = host(fl.fp8_scaled_mm(dev(qa), dev(qw), scalar(0.5), dev(sw), out_dtype=torch.bfloat16,
+                              kernel="stream"))
     exact = oracle.scaled_mm_bruteforce(qa, qw, np.float32(0.5), sw)
     want = torch.from_numpy(exact).to(torch.bfloat16).float().numpy()
     assert np.array_equal(y, want)
@@ -168,7 +172,8 @@ def test_w8a16_chain_with_stable_weights(stable):
     assert_gemm_close(host(y2), oracle.w8a16_ref(y1_f16, q2, s2))
 
 
-def test_w8a8_small_m_chain_with_stable_weights():
+@pytest.mark.parametrize("kernel", ["stream", "swapped"])
+def test_w8a8_small_m_chain_with_stable_weights(kernel):
     # quantize -> product -> quantize its output -> product, all with the flag
     M, K, N = 8, 4096, 4096
     x = synthetic.activation(M, K, torch.bfloat16, seed=81)
@@ -177,9 +182,11 @@ def test_w8a8_small_m_chain_with_stable_weights():
     q1, s1 = oracle.quant_per_row(w1)
     q2, s2 = oracle.quant_per_row(w2)
     qa, sa = fl.fp8_quant_per_tensor(dev(x))
-    y1 = fl.fp8_scaled_mm(qa, dev(q1), sa, dev(s1), out_dtype=torch.bfloat16, stable_weights=True)
+    y1 = fl.fp8_scaled_mm(qa, dev(q1), sa, dev(s1), out_dtype=torch.bfloat16, stable_weights=True,
+                          kernel=kernel)
     qb, sb = fl.fp8_quant_per_tensor(y1)
-    y2 = fl.fp8_scaled_mm(qb, dev(q2), sb, dev(s2), out_dtype=torch.bfloat16, stable_weights=True)
+    y2 = fl.fp8_scaled_mm(qb, dev(q2), sb, dev(s2), out_dtype=torch.bfloat16, stable_weights=True,
+                          kernel=kernel)
     qa_o, sa_o = oracle.quant_per_tensor(x)
     assert np.array_equal(host(qa), qa_o)
     assert_gemm_close(host(y1), oracle.scaled_mm_ref(qa_o, q1, sa_o, s1))
@@ -189,8 +196,9 @@ def test_w8a8_small_m_chain_with_stable_weights():
     assert_gemm_close(host(y2), oracle.scaled_mm_ref(qb_o, q2, sb_o, s2))
 
 
+@pytest.mark.parametrize("kernel", ["stream", "swapped"])
 @pytest.mark.parametrize("M", [1, 8, 16])
-def test_w8a8_small_m_graph_replay_with_stable_weights(M):
+def test_w8a8_small_m_graph_replay_with_stable_weights(M, kernel):
     # quantize -> product -> quantize -> product in one CUDA graph, the
     # products launched as programmatic dependents: each reads codes and a
     # scale the kernel before it writes.  Every intermediate is zeroed before
@@ -211,10 +219,10 @@ def test_w8a8_small_m_graph_replay_with_stable_weights(M):
     def step():
         fl.fp8_quant_per_tensor(xd, q=qa, scale=sa, ws=ws)
         fl.fp8_scaled_mm(qa, q1d, sa, s1d, out_dtype=torch.bfloat16, y=y1, ws=ws,
-                         stable_weights=True)
+                         stable_weights=True, kernel=kernel)
         fl.fp8_quant_per_tensor(y1, q=qb, scale=sb, ws=ws)
         fl.fp8_scaled_mm(qb, q2d, sb, s2d, out_dtype=torch.bfloat16, y=y2, ws=ws,
-                         stable_weights=True)
+                         stable_weights=True, kernel=kernel)
 
     step()
     torch.cuda.synchronize()
@@ -280,7 +288,7 @@ def test_w8a16_large_n_token_groups(M, N, K, xdtype):
 
 @pytest.mark.parametrize("out", ["bf16", "e4m3"])
 def test_w8a8_small_m_large_n(out):
-    _w8a8_small(16, 10240, 1024, True, out, seed=123)
+    _w8a8_small(16, 10240, 1024, True, out, seed=123, kernel="stream")
 
 
 def _packed_layout_reference(qw):

@@ -33,8 +33,10 @@ def _operands(M, N, K, seed):
     return qa, sa, qw, sw
 
 
-@pytest.mark.parametrize("M", [256, 64])  # persistent tiles; cluster split-K
-def test_product_wait_times_out_then_recovers(M):
+# persistent tiles; cluster split-K; swapped operands with and without a
+# cluster splitting K
+@pytest.mark.parametrize("M,kernel", [(256, "auto"), (64, "auto"), (64, "swapped"), (8, "swapped")])
+def test_product_wait_times_out_then_recovers(M, kernel):
     N, K = 512, 1024
     qa, sa, qw, sw = _operands(M, N, K, seed=900 + M)
     ws = fl.workspace(DEV)
@@ -43,12 +45,12 @@ def test_product_wait_times_out_then_recovers(M):
     sa_d = torch.tensor([sa], dtype=torch.float32, device=DEV)
     sw_d = torch.tensor([sw], dtype=torch.float32, device=DEV)
     fl.fp8l_debug_waits(SHORT, fl._binding.STALL_MMA)
-    fl.fp8_scaled_mm(a, w, sa_d, sw_d, out_dtype=torch.bfloat16, ws=ws)
+    fl.fp8_scaled_mm(a, w, sa_d, sw_d, out_dtype=torch.bfloat16, ws=ws, kernel=kernel)
     torch.cuda.synchronize()
     assert fl.fp8l_read_status(ws) == fl._binding.ETIMEOUT
     # the workspace was reset with the status: the next ordinary call is exact
     fl.fp8l_debug_waits(0, 0)
-    y = fl.fp8_scaled_mm(a, w, sa_d, sw_d, out_dtype=torch.bfloat16, ws=ws)
+    y = fl.fp8_scaled_mm(a, w, sa_d, sw_d, out_dtype=torch.bfloat16, ws=ws, kernel=kernel)
     assert fl.fp8l_read_status(ws) == fl._binding.OK
     y_ref = scaled_mm_ref_rows(qa, qw, sa, [sw])
     assert_gemm_close(host(y), y_ref, "after a time-out")
