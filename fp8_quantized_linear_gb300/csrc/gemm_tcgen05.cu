@@ -75,6 +75,12 @@ struct GemmParams {
     long long wait_cycles;  // limit of the main waits (kDefaultWaitCycles unless a test shortened it)
     unsigned stall;         // kStallMma: testing the time-out path
     int split;  // > 1: a cluster of `split` CTAs shares one tile and splits its k-blocks
+    // CTA-pair kernel: 256 x 256 tiles over the columns [0, pair_n_main)
+    // (pair_main_tiles of them), then pair_tail_n columns of tiles
+    // pair_tail_w wide over [pair_n_main, N) so that the last round of tiles
+    // spreads over the SM pairs (pair_tail_n = 0: 256-wide tiles throughout)
+    int pair_main_tiles, pair_n_main, pair_tail_w, pair_tail_n;
+    uint32_t idesc_tail;  // instruction descriptor of the tail tiles (N = pair_tail_w)
 };
 
 // Instruction descriptor, kind::f8f6f4: D f32 (bits 4-5 = 1), A and B E4M3
@@ -521,13 +527,34 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
 }
 
 __device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                            uint32_t accumulate) {
+                                            uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(kIdescPair), "r"(accumulate)
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// Where a pair tile sits: 256-row block mt, first column n0, width w (256,
+// or the tail width).
+struct PairTile {
+    int mt, n0, w;
+};
+
+__device__ __forceinline__ PairTile pair_tile(const GemmParams &p, int tile, int tiles_m) {
+    PairTile t;
+    if (tile < p.pair_main_tiles) {
+        t.mt = tile % tiles_m;
+        t.n0 = (tile / tiles_m) * P_BN;
+        t.w = P_BN;
+    } else {
+        const int u = tile - p.pair_main_tiles;
+        t.mt = u % tiles_m;
+        t.n0 = p.pair_n_main + (u / tiles_m) * p.pair_tail_w;
+        t.w = p.pair_tail_w;
+    }
+    return t;
 }
 
 // arrive on the barrier at this offset in both CTAs once the MMAs issued so
@@ -542,7 +569,8 @@ __device__ __forceinline__ void commit_pair(uint32_t bar) {
 
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_f8_pair(const __grid_constant__ CUtensorMap tmap_a,
-             const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+             const __grid_constant__ CUtensorMap tmap_b,
+             const __grid_constant__ CUtensorMap tmap_bt, const GemmParams p) {
     asm volatile("griddepcontrol.wait;" ::: "memory");  // see gemm_f8_tcgen05
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -594,19 +622,23 @@ gemm_f8_pair(const __grid_constant__ CUtensorMap tmap_a,
     const int pair = static_cast<int>(blockIdx.x) >> 1;
     const int num_pairs = static_cast<int>(gridDim.x) >> 1;
     const int tiles_m = (p.M + 2 * P_BM - 1) / (2 * P_BM);
-    const int num_tiles = tiles_m * p.num_n_blocks;
+    const int num_tiles = p.pair_main_tiles + tiles_m * p.pair_tail_n;
 
     if (warp == 0) {
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
+            if (p.pair_tail_n > 0)
+                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_bt)) : "memory");
             int stage = 0;
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;  // even CTA: stages armed, their parity
             bool ok = true;
             for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
-                const int mt = tile % tiles_m;
-                const int nt = tile / tiles_m;
+                const PairTile t = pair_tile(p, tile, tiles_m);
+                const bool tail = t.w != P_BN;
+                // bytes of one stage in each CTA: its A rows and its half of the tile's columns
+                const uint32_t stage_tx = kPABytes + static_cast<uint32_t>(t.w / 2) * BK;
                 for (int kb = 0; kb < p.num_k_blocks; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.wait_cycles,
                                    peer_abort)) {
@@ -615,14 +647,14 @@ gemm_f8_pair(const __grid_constant__ CUtensorMap tmap_a,
                     }
                     const uint32_t sa = sbase + stage * kPStageBytes;
                     if (leader) {
-                        mbar_expect_tx(full_bar(stage), 2 * kPStageBytes);
+                        mbar_expect_tx(full_bar(stage), 2 * stage_tx);
                         armed |= 1u << stage;
                         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     }
                     const uint32_t fb = map_to_rank(full_bar(stage), 0);
-                    tma_load_2d_pair(sa, &tmap_a, kb * BK, mt * 2 * P_BM + static_cast<int>(rank) * P_BM, fb);
-                    tma_load_2d_pair(sa + kPABytes, &tmap_b, kb * BK,
-                                     nt * P_BN + static_cast<int>(rank) * (P_BN / 2), fb);
+                    tma_load_2d_pair(sa, &tmap_a, kb * BK, t.mt * 2 * P_BM + static_cast<int>(rank) * P_BM, fb);
+                    tma_load_2d_pair(sa + kPABytes, tail ? &tmap_bt : &tmap_b, kb * BK,
+                                     t.n0 + static_cast<int>(rank) * (t.w / 2), fb);
                     if (++stage == P_STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -650,6 +682,7 @@ gemm_f8_pair(const __grid_constant__ CUtensorMap tmap_a,
                                peer_abort))
                     break;
                 tc_fence_after();
+                const uint32_t idesc = tile < p.pair_main_tiles ? kIdescPair : p.idesc_tail;
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * P_BN);
                 for (int kb = 0; kb < p.num_k_blocks; ++kb) {
                     if (!mbar_wait_fast(full_bar(stage), phase, abort_flag, p.status, p.wait_cycles,
@@ -662,7 +695,7 @@ gemm_f8_pair(const __grid_constant__ CUtensorMap tmap_a,
                     const uint64_t da = sw128_desc(sa), db = sw128_desc(sa + kPABytes);
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k)
-                        mma_f8_pair(d_tmem, da + 2 * k, db + 2 * k, (kb | k) != 0 ? 1u : 0u);
+                        mma_f8_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
                     commit_pair(empty_bar(stage));
                     if (++stage == P_STAGES) {
                         stage = 0;
@@ -688,22 +721,21 @@ gemm_f8_pair(const __grid_constant__ CUtensorMap tmap_a,
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = pair; tile < num_tiles; tile += num_pairs) {
-            const int mt = tile % tiles_m;
-            const int nt = tile / tiles_m;
+            const PairTile t = pair_tile(p, tile, tiles_m);
             if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status, p.wait_cycles, peer_abort))
                 break;
             tc_fence_after();
-            const int m = mt * 2 * P_BM + row;
+            const int m = t.mt * 2 * P_BM + row;
             const bool row_ok = m < p.M;
             const float sa = p.a_per_token ? (row_ok ? __ldg(p.a_scale + m) : 0.0f) : sa0;
             const float sa_sw = sa * sw0;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * P_BN);
 #pragma unroll 1
-            for (int c = 0; c < P_BN / 32; ++c) {
+            for (int c = 0; c < t.w / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld32(taddr + static_cast<uint32_t>(c * 32), r);
-                const int n0 = nt * P_BN + c * 32;
+                const int n0 = t.n0 + c * 32;
                 if (row_ok && n0 < p.N) store_row_chunk(p, r, m, n0, sa, sa_sw, p.w_scale);
             }
             tc_fence_before();
@@ -755,6 +787,55 @@ int ensure_smem_attr() {
     return FP8L_OK;
 }
 
+// Tile plan of the CTA-pair kernel.  256 x 256 tiles fill whole rounds of
+// the SM pairs; the columns left over become tiles a multiple of 32 narrower
+// so that the last round spreads over the pairs instead of leaving most of
+// them idle (M = 1024, N = 10240: 160 tiles on 76 pairs would take three
+// rounds, the third with 8 tiles).  Cost model: a tile w columns wide costs
+// max(w, kTailFloor) / 256 of a full tile (its A tile is loaded whatever its
+// width); the plan minimises the most loaded pair's cost, widest tail first
+// among equals, and keeps 256-wide tiles throughout unless that is beaten.
+constexpr int kTailFloor = 96;
+
+struct PairPlan {
+    int main_tiles, n_main, tail_w, tail_n;
+};
+
+PairPlan plan_pair(int tiles_m, int N, int pairs) {
+    const int nb = (N + P_BN - 1) / P_BN;
+    const int total = tiles_m * nb;
+    PairPlan best{total, nb * P_BN, 0, 0};
+    auto cost = [&](int main_tiles, int tail_tiles, int w) {
+        const int mr = main_tiles % pairs, tr = tail_tiles % pairs;
+        const int wc = w > kTailFloor ? w : kTailFloor;
+        int worst = 0;  // in 1/256 of a full tile
+        for (int q = 0; q < pairs; ++q) {
+            const int mc = main_tiles / pairs + (q < mr ? 1 : 0);
+            const int d = (q - mr + pairs) % pairs;  // tail tiles start after the last main one
+            const int tc = tail_tiles / pairs + (d < tr ? 1 : 0);
+            const int c = mc * P_BN + tc * wc;
+            worst = c > worst ? c : worst;
+        }
+        return worst;
+    };
+    if (pairs < 1 || total % pairs == 0) return best;
+    int best_cost = cost(total, 0, P_BN);
+    const int rounds = total / pairs;
+    int c = (rounds * pairs) / tiles_m;  // whole 256-column blocks before the tail
+    if (c > nb) c = nb;
+    const int rem = N - c * P_BN;
+    if (rem <= 0) return best;
+    for (int w = P_BN - 32; w >= 32; w -= 32) {
+        const int tail_n = (rem + w - 1) / w;
+        const int cst = cost(c * tiles_m, tail_n * tiles_m, w);
+        if (cst < best_cost) {
+            best_cost = cst;
+            best = PairPlan{c * tiles_m, c * P_BN, w, tail_n};
+        }
+    }
+    return best;
+}
+
 // groups == 0: one product of w [N, K]; groups > 0: w is [groups, N, K] and
 // group_offs the device row offsets of the experts (grouped mode).  Products
 // with enough tiles to fill the SMs run the CTA-pair kernel unless
@@ -792,8 +873,24 @@ int launch_tcgen05(const uint8_t *a, const uint8_t *w, int M, int N, int K, cons
     const WaitConfig wc = wait_config();
     p.wait_cycles = wc.cycles;
     p.stall = wc.stall;
+    p.pair_main_tiles = 0;
+    p.pair_n_main = 0;
+    p.pair_tail_w = 0;
+    p.pair_tail_n = 0;
+    p.idesc_tail = 0;
     if (pair_ok) {
-        const int64_t pair_tiles = int64_t((M + 2 * P_BM - 1) / (2 * P_BM)) * p.num_n_blocks;
+        const int tiles_m = (M + 2 * P_BM - 1) / (2 * P_BM);
+        const PairPlan plan = plan_pair(tiles_m, N, sms / 2);
+        p.pair_main_tiles = plan.main_tiles;
+        p.pair_n_main = plan.n_main;
+        p.pair_tail_w = plan.tail_w;
+        p.pair_tail_n = plan.tail_n;
+        // kind::f8f6f4, D f32, E4M3 K-major operands, N = tail width, M = 256
+        p.idesc_tail = (1u << 4) | (static_cast<uint32_t>(plan.tail_w >> 3) << 17) |
+                       (static_cast<uint32_t>(256 >> 4) << 24);
+        CUtensorMap mbt = mb;
+        if (plan.tail_n > 0 && make_map(&mbt, w, N, K, plan.tail_w / 2) != FP8L_OK) return FP8L_ECUDA;
+        const int64_t pair_tiles = int64_t(plan.main_tiles) + int64_t(tiles_m) * plan.tail_n;
         const int64_t pairs = pair_tiles < sms / 2 ? pair_tiles : sms / 2;
         p.split = 1;
         cudaLaunchConfig_t cfg = {};
@@ -810,7 +907,7 @@ int launch_tcgen05(const uint8_t *a, const uint8_t *w, int M, int N, int K, cons
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = pdl ? 2 : 1;
-        if (cudaLaunchKernelEx(&cfg, gemm_f8_pair, ma, mb, p) != cudaSuccess) return FP8L_ECUDA;
+        if (cudaLaunchKernelEx(&cfg, gemm_f8_pair, ma, mb, mbt, p) != cudaSuccess) return FP8L_ECUDA;
         return launch_status();
     }
     // grouped: each expert adds at most one partial block to ceil(M / BM)

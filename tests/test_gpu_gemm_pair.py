@@ -1,6 +1,7 @@
 """GPU parity of the two tile shapes of the tcgen05 product: 256 x 256 tiles
 spanning a pair of SMs (tcgen05.mma.cta_group::2, the default when the
-product has enough tiles) and 128 x 256 tiles on one SM each
+product has enough tiles; the columns left after the last whole round of
+tiles run as narrower tail tiles) and 128 x 256 tiles on one SM each
 (FP8L_SINGLE_SM_TILES).  Both against the CPU oracle: exact-integer products
 bit for bit, permutation weights exactly, and Gaussian operands within the
 layer's tolerance, with ragged M and N tails of the 256-row pair tiles."""
@@ -30,6 +31,27 @@ def test_exact_integer(M, N, K, single_sm):
     y = host(fl.fp8_scaled_mm(dev(qa), dev(qw), scalar(0.5), dev(sw), out_dtype=torch.bfloat16,
                               single_sm=single_sm))
     rows = sample_rows(M, 160, seed=M)
+    exact = oracle.scaled_mm_ref(qa[rows], qw, np.float32(0.5), sw)
+    want = torch.from_numpy(exact).to(torch.bfloat16).float().numpy()
+    bad = np.argwhere(y[rows] != want)
+    assert bad.size == 0, (bad[:5],)
+    assert_status_ok()
+
+
+# the pair kernel's tile plans: 256 x 256 tiles in whole rounds, then the
+# left-over columns as narrower tiles (widths 96, 128, 192 and 224 here,
+# and 224 throughout when the tiles are fewer than the SM pairs), with
+# ragged ends of N inside the last tail tile
+@pytest.mark.parametrize("M,N,K", [(1024, 10240, 256), (1024, 8192, 384), (1024, 4096, 512),
+                                   (4096, 10240, 128), (4096, 8192, 128), (1000, 11008, 256),
+                                   (4097, 1040, 384)])
+def test_tail_tiles_exact_integer(M, N, K):
+    rng = np.random.default_rng(M * 3 + N + K)
+    qa = CODES[rng.integers(0, 7, (M, K))]
+    qw = CODES[rng.integers(0, 7, (N, K))]
+    sw = np.array([2.0 ** (n % 7 - 3) for n in range(N)], np.float32)
+    y = host(fl.fp8_scaled_mm(dev(qa), dev(qw), scalar(0.5), dev(sw), out_dtype=torch.bfloat16))
+    rows = sample_rows(M, 96, seed=N)
     exact = oracle.scaled_mm_ref(qa[rows], qw, np.float32(0.5), sw)
     want = torch.from_numpy(exact).to(torch.bfloat16).float().numpy()
     bad = np.argwhere(y[rows] != want)
