@@ -10,6 +10,7 @@ carry the C entry points' names:
   fp8_scaled_mm         W8A8 scaled product (tcgen05 products; few tokens and
                         small weights streamed on the CUDA cores)
   scaled_mm_kernel      which of the three kernels fp8_scaled_mm runs for a shape
+  w8a16_mm_kernel       which of the two kernels fp8_w8a16_mm runs
   fp8_grouped_mm        W8A8 products of mixture-of-experts layers (device offsets)
   fp8_w8a16_mm          weight-only fp16/bf16 x E4M3 product
   fp8_pack_w8a16_weights  weights permuted once into the order that product
@@ -21,4 +22,4 @@ from ._binding import (  # noqa: F401
     BF16, E4M3, F16, F32, Fp8LinearError, LIB_PATH, fp8_grouped_mm, fp8_pack_w8a16_weights,
     fp8_packed_weight_bytes, fp8_quant_per_row, fp8_quant_per_tensor, fp8_scaled_mm,
     fp8_rmsnorm_quant, fp8_w8a16_mm, fp8l_debug_waits, fp8l_read_status, fp8l_workspace_bytes, load,
-    scaled_mm_kernel, strerror, workspace)
+    scaled_mm_kernel, strerror, w8a16_mm_kernel, workspace)

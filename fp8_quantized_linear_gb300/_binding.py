@@ -74,6 +74,8 @@ def load():
         lib.fp8_quant_per_row.argtypes = [P, I, I64, I64, P, P, P]
         lib.fp8_scaled_mm.restype = I
         lib.fp8_scaled_mm.argtypes = [P, P, I64, I64, I64, P, P, I, P, P, I, P, ctypes.c_uint, P]
+        lib.fp8_w8a16_mm_kernel.restype = ctypes.c_uint
+        lib.fp8_w8a16_mm_kernel.argtypes = [I64, I64, I64, ctypes.c_uint]
         lib.fp8_scaled_mm_kernel.restype = ctypes.c_uint
         lib.fp8_scaled_mm_kernel.argtypes = [I64, I64, I64, ctypes.c_uint]
         lib.fp8_w8a16_mm.restype = I
@@ -239,6 +241,13 @@ def scaled_mm_kernel(M: int, N: int, K: int, kernel: str = "auto") -> str:
     return {v: k for k, v in KERNELS.items()}[code]
 
 
+def w8a16_mm_kernel(M: int, N: int, K: int, kernel: str = "auto") -> str:
+    """Name ("stream" or "swapped") of the kernel fp8_w8a16_mm runs for this
+    shape and kernel choice (fp8_w8a16_mm_kernel; no GPU needed)."""
+    code = load().fp8_w8a16_mm_kernel(M, N, K, KERNELS[kernel])
+    return {v: k for k, v in KERNELS.items()}[code]
+
+
 def fp8_scaled_mm(a: torch.Tensor, w: torch.Tensor, a_scale: torch.Tensor,
                   w_scale: torch.Tensor, out_dtype=torch.bfloat16,
                   out_scale: torch.Tensor | None = None, y: torch.Tensor | None = None,
@@ -348,12 +357,13 @@ def fp8_pack_w8a16_weights(w: torch.Tensor, out: torch.Tensor | None = None) -> 
 
 def fp8_w8a16_mm(x: torch.Tensor, w: torch.Tensor, w_scale: torch.Tensor,
                  y: torch.Tensor | None = None, stable_weights: bool = False,
-                 packed: bool = False) -> torch.Tensor:
+                 packed: bool = False, kernel: str = "auto") -> torch.Tensor:
     """Weight-only product: fp16/bf16 x [M, K] times E4M3 w [N, K] with
     per-channel w_scale [N]; the output has x's dtype.  stable_weights sets
     FP8L_WEIGHTS_STABLE (no work in flight on the stream writes w or
     w_scale).  packed: w is the output of fp8_pack_w8a16_weights (N is
-    taken from w_scale) and FP8L_WEIGHTS_PACKED is set."""
+    taken from w_scale) and FP8L_WEIGHTS_PACKED is set.  kernel ("auto",
+    "stream" or "swapped") sets the FP8L_KERNEL_* choice."""
     _need_cuda(x, w, w_scale, y)
     w = _codes(w)
     M, K = x.shape
@@ -365,7 +375,8 @@ def fp8_w8a16_mm(x: torch.Tensor, w: torch.Tensor, w_scale: torch.Tensor,
         raise ValueError("shape mismatch")
     if y is None:
         y = torch.empty((M, N), dtype=x.dtype, device=x.device)
-    flags = (WEIGHTS_STABLE if stable_weights else 0) | (WEIGHTS_PACKED if packed else 0)
+    flags = ((WEIGHTS_STABLE if stable_weights else 0) | (WEIGHTS_PACKED if packed else 0) |
+             KERNELS[kernel])
     with torch.cuda.device(x.device):
         st = load().fp8_w8a16_mm(x.data_ptr(), _DTYPE_CODE[x.dtype], w.data_ptr(),
                                  w_scale.data_ptr(), M, N, K, y.data_ptr(), flags,

@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -76,6 +77,68 @@ int make_kmajor_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, 
     return r == CUDA_SUCCESS ? FP8L_OK : FP8L_ECUDA;
 }
 
+namespace {
+// Status word of the calls that take no workspace (fp8_w8a16_mm's
+// tensor-core kernel): time-outs are recorded here and reported, then
+// cleared, by fp8l_read_status together with the workspace's word.
+__device__ unsigned g_library_status;
+
+struct StatusSlot {
+    std::mutex mu;
+    unsigned long long ctx_id = 0;  // context the address below belongs to
+    unsigned *ptr = nullptr;
+};
+constexpr int kStatusMaxDevices = 64;
+StatusSlot g_status_slots[kStatusMaxDevices];
+}  // namespace
+
+// Device address of g_library_status in the context current on this thread
+// (taken with cudaGetSymbolAddress, kept per device with the id of its
+// context and looked up again when another context is current).
+int library_status_word(unsigned **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FP8L_ECUDA;
+    if (dev < 0 || dev >= kStatusMaxDevices) return FP8L_EUNSUPPORTED;
+    StatusSlot &slot = g_status_slots[dev];
+    std::lock_guard<std::mutex> lock(slot.mu);
+    unsigned long long id = 0;
+    if (current_context_id(&id) != FP8L_OK) return FP8L_ECUDA;
+    if (slot.ptr == nullptr || id == 0 || id != slot.ctx_id) {
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_library_status) != cudaSuccess || addr == nullptr)
+            return FP8L_ECUDA;
+        if (current_context_id(&id) != FP8L_OK || id == 0) return FP8L_ECUDA;
+        slot.ptr = static_cast<unsigned *>(addr);
+        slot.ctx_id = id;
+    }
+    *out = slot.ptr;
+    return FP8L_OK;
+}
+
+int make_tile_map(CUtensorMap *map, const void *ptr, int elem_bytes, int rank, const uint64_t *dims,
+                  const uint64_t *strides, const uint32_t *box, bool swizzle128) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (enc == nullptr || rank < 1 || rank > 5 || (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 8))
+        return FP8L_ECUDA;
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], estr[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = static_cast<cuuint64_t>(dims[i]);
+        b[i] = static_cast<cuuint32_t>(box[i]);
+        estr[i] = 1;
+        if (i + 1 < rank) st[i] = static_cast<cuuint64_t>(strides[i]);
+    }
+    const CUtensorMapDataType type = elem_bytes == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                     : elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
+                                                       : CU_TENSOR_MAP_DATA_TYPE_UINT64;
+    CUresult r = enc(map, type,
+                     static_cast<cuuint32_t>(rank), const_cast<void *>(ptr), d, st, b, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8L_OK : FP8L_ECUDA;
+}
+
 int current_context_id(unsigned long long *id) {
     static std::atomic<PFN_cuCtxGetCurrent_v4000> get_cur{nullptr};
     static std::atomic<PFN_cuCtxGetId_v12000> get_id{nullptr};
@@ -111,17 +174,21 @@ namespace {
 // zeroed too (ticket, call counter, arrival counts, maximum words), since the
 // call that gave up may have left them part-way through a grid barrier.
 int read_and_clear(void *ws, cudaStream_t s) {
-    unsigned host = 0;
+    unsigned host[2] = {0u, 0u};
     unsigned *dev = status_word(ws);
-    if (cudaMemcpyAsync(&host, dev, sizeof(unsigned), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    unsigned *lib = nullptr;
+    if (library_status_word(&lib) != FP8L_OK) return FP8L_ECUDA;
+    if (cudaMemcpyAsync(&host[0], dev, sizeof(unsigned), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(&host[1], lib, sizeof(unsigned), cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return FP8L_ECUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return FP8L_ECUDA;
-    if (host != 0u) {
-        const size_t bytes = (host & kStatusTimeout) ? kBarrierAreaBytes : sizeof(unsigned);
+    if (host[0] != 0u) {
+        const size_t bytes = (host[0] & kStatusTimeout) ? kBarrierAreaBytes : sizeof(unsigned);
         if (cudaMemsetAsync(ws, 0, bytes, s) != cudaSuccess) return FP8L_ECUDA;
-        if (cudaStreamSynchronize(s) != cudaSuccess) return FP8L_ECUDA;
     }
-    return (host & kStatusTimeout) ? FP8L_ETIMEOUT : FP8L_OK;
+    if (host[1] != 0u && cudaMemsetAsync(lib, 0, sizeof(unsigned), s) != cudaSuccess) return FP8L_ECUDA;
+    if ((host[0] | host[1]) != 0u && cudaStreamSynchronize(s) != cudaSuccess) return FP8L_ECUDA;
+    return ((host[0] | host[1]) & kStatusTimeout) ? FP8L_ETIMEOUT : FP8L_OK;
 }
 }  // namespace
 

@@ -91,6 +91,18 @@ int current_context_id(unsigned long long *id);
 int make_kmajor_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_k,
                     int box_rows);
 
+// Device address (in the current context) of the library's own status word,
+// where kernels of calls without a workspace record time-outs;
+// fp8l_read_status reports and clears it with the workspace's word.
+int library_status_word(unsigned **out);
+
+// N-D TMA map (rank <= 5) over 1-, 2- or 8-byte elements: dims and box
+// innermost first, strides[i] = bytes between consecutive indices of
+// dimension i + 1 (multiples of 16); optional 128-byte swizzle; zero fill
+// outside the tensor.
+int make_tile_map(CUtensorMap *map, const void *ptr, int elem_bytes, int rank, const uint64_t *dims,
+                  const uint64_t *strides, const uint32_t *box, bool swizzle128);
+
 // FP8L_ECUDA if the last launch failed, else FP8L_OK.
 inline int launch_status() {
     return cudaGetLastError() == cudaSuccess ? FP8L_OK : FP8L_ECUDA;
@@ -101,6 +113,9 @@ int launch_skinny_e4m3(const uint8_t *a, const uint8_t *w, int M, int N, int K,
                        const float *a_scale, int a_per_token, const float *w_scale,
                        int w_per_channel, const float *out_scale, void *y, int out_dtype,
                        bool stable_weights, cudaStream_t stream);
+int launch_w8a16_tc(const void *x, int x_dtype, const uint8_t *w, bool packed, const float *w_scale,
+                    int M, int N, int K, void *y, unsigned *status, int sms, bool stable,
+                    cudaStream_t stream);
 int launch_swapab(const uint8_t *a, const uint8_t *w, int M, int N, int K, const float *a_scale,
                   int a_per_token, const float *w_scale, int w_per_channel,
                   const float *out_scale, void *y, int out_dtype, unsigned *status, int sms,

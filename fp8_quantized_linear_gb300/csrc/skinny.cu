@@ -378,12 +378,31 @@ extern "C" int fp8_pack_w8a16_weights(const uint8_t *w, int64_t N, int64_t K, ui
     return launch_status();
 }
 
+// The kernel fp8_w8a16_mm runs for FP8L_KERNEL_AUTO: the CUDA-core kernel up
+// to 16 tokens (0.45-0.82 of HBM on the decode shapes, against 0.26-0.50
+// for the tensor-core product); from 17 to 64 tokens the tensor-core
+// product (weights widened in TMEM, tokens as the MMA's N side), which
+// streams the weights once whatever the token count (0.24-0.48 of HBM at
+// 32-64 tokens against 0.15-0.33 for the CUDA-core kernel, whose token
+// groups of 16 each re-read W).
+extern "C" unsigned fp8_w8a16_mm_kernel(int64_t M, int64_t N, int64_t K, unsigned flags) {
+    (void)N;
+    (void)K;
+    const unsigned k = flags & FP8L_KERNEL_MASK;
+    if (k != FP8L_KERNEL_AUTO) return k;
+    return (M >= 17 && M <= 64) ? FP8L_KERNEL_SWAPPED : FP8L_KERNEL_STREAM;
+}
+
 extern "C" int fp8_w8a16_mm(const void *x, int x_dtype, const uint8_t *w, const float *w_scale,
                             int64_t M, int64_t N, int64_t K, void *y, unsigned flags,
                             void *stream) {
     using namespace fp8l;
     if (x_dtype != FP8L_F16 && x_dtype != FP8L_BF16) return FP8L_EINVAL;
-    if ((flags & ~(FP8L_WEIGHTS_STABLE | FP8L_WEIGHTS_PACKED)) != 0u) return FP8L_EINVAL;
+    if ((flags & ~(FP8L_WEIGHTS_STABLE | FP8L_WEIGHTS_PACKED | FP8L_KERNEL_MASK)) != 0u)
+        return FP8L_EINVAL;
+    const unsigned kernel = fp8_w8a16_mm_kernel(M, N, K, flags);
+    if (kernel == FP8L_KERNEL_TILED) return FP8L_EINVAL;
+    if (kernel == FP8L_KERNEL_SWAPPED && M > 64) return FP8L_ESHAPE;
     if (M < 0 || M > 0x7FFFFFFF || N <= 0 || K <= 0 || N > (1 << 20) || K > (1 << 20) ||
         N % 16 != 0 || K % 16 != 0)
         return FP8L_ESHAPE;
@@ -392,8 +411,17 @@ extern "C" int fp8_w8a16_mm(const void *x, int x_dtype, const uint8_t *w, const 
     if (!aligned16(w) || (M > 0 && (!aligned16(x) || !aligned16(y))) ||
         (reinterpret_cast<uintptr_t>(w_scale) & 3u) != 0)
         return FP8L_EALIGN;
-    int st = check_device(nullptr);
+    int sms = 0;
+    int st = check_device(&sms);
     if (st != FP8L_OK) return st;
+    if (M == 0) return FP8L_OK;
+    if (kernel == FP8L_KERNEL_SWAPPED) {
+        unsigned *status = nullptr;
+        if (library_status_word(&status) != FP8L_OK) return FP8L_ECUDA;
+        return launch_w8a16_tc(x, x_dtype, w, (flags & FP8L_WEIGHTS_PACKED) != 0u, w_scale,
+                               static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), y, status,
+                               sms, (flags & FP8L_WEIGHTS_STABLE) != 0u, as_stream(stream));
+    }
     SkinnyArgs args{w, x, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
                     nullptr, 0, w_scale, 1, nullptr, y, x_dtype};
     const bool stable = (flags & FP8L_WEIGHTS_STABLE) != 0u;

@@ -32,8 +32,9 @@
  *  - Errors found on the host (FP8L_EINVAL, FP8L_ESHAPE, FP8L_EALIGN,
  *    FP8L_EUNSUPPORTED) are returned before anything is launched and leave
  *    every output untouched.  FP8L_ECUDA reports a failed CUDA call or
- *    launch.  Device-side wait time-outs are recorded in the workspace and
- *    reported by fp8l_read_status().
+ *    launch.  Device-side wait time-outs are recorded in the workspace (or,
+ *    for fp8_w8a16_mm, in a status word of the library) and reported by
+ *    fp8l_read_status().
  *  - Inputs must be finite.  NaN or Inf input is outside the contract.
  */
 #ifndef FP8LINEAR_H
@@ -226,13 +227,26 @@ FP8L_API unsigned fp8_scaled_mm_kernel(int64_t M, int64_t N, int64_t K, unsigned
  * with FP8L_WEIGHTS_PACKED the packed layout of them
  * (fp8_pack_w8a16_weights; the result is bit-for-bit the same);
  * w_scale: [N] floats; y: [M, N] of x_dtype.  M >= 0; N and K positive
- * multiples of 16, at most 2^20.  Built for decode batches (M <= 16); a
- * larger M is computed correctly in groups of 16 rows, each group
- * re-reading W.  flags: any of FP8L_WEIGHTS_STABLE and FP8L_WEIGHTS_PACKED
- * (other bits are FP8L_EINVAL). */
+ * multiples of 16, at most 2^20.  Built for decode batches.  Kernels
+ * (fp8_w8a16_mm_kernel names the one a call runs): up to 16 tokens, and
+ * above 64, a weight-streaming kernel on the CUDA cores (a larger M is
+ * computed correctly in groups of 16 rows, each group re-reading W); from
+ * 17 to 64 tokens a tcgen05 product that widens the weights to x_dtype
+ * (exactly) into tensor memory, 128 weight rows by the tokens per tile.  The
+ * tcgen05 kernel's device-side waits are bounded; a time-out is recorded in
+ * a status word held by the library (this call takes no workspace) and
+ * reported by the next fp8l_read_status.  flags: any of
+ * FP8L_WEIGHTS_STABLE and FP8L_WEIGHTS_PACKED, and FP8L_KERNEL_STREAM or
+ * FP8L_KERNEL_SWAPPED (the tcgen05 kernel; FP8L_ESHAPE above 64 tokens);
+ * other bits, and FP8L_KERNEL_TILED, are FP8L_EINVAL. */
 FP8L_API int fp8_w8a16_mm(const void *x, int x_dtype, const uint8_t *w,
                  const float *w_scale, int64_t M, int64_t N, int64_t K,
                  void *y, unsigned flags, void *stream);
+
+/* The kernel fp8_w8a16_mm runs for this shape and these flags:
+ * FP8L_KERNEL_STREAM or FP8L_KERNEL_SWAPPED (the flags' own choice when
+ * they make one).  A pure function of its arguments; needs no GPU. */
+FP8L_API unsigned fp8_w8a16_mm_kernel(int64_t M, int64_t N, int64_t K, unsigned flags);
 
 /* Grouped W8A8 product for mixture-of-experts layers ("RFC: FP8
  * Quantization Schema in vLLM", the gate_proj question: FP8 products need
@@ -356,10 +370,14 @@ FP8L_API int fp8_quant_per_tensor_noalloc(const void *x, int x_dtype, int64_t ro
                                           int64_t cols, uint8_t *q, float *scale,
                                           void *stream);
 
-/* Waits for `stream`, then reads and clears the workspace's status word.
- * Returns FP8L_OK, FP8L_ETIMEOUT if a device-side wait of an earlier call
- * gave up (that call's outputs are then undefined; the workspace's barrier
- * words are zeroed as well, so the next call starts clean), or FP8L_ECUDA. */
+/* Waits for `stream`, then reads and clears the workspace's status word and
+ * the library's own status word on the current device (where
+ * fp8_w8a16_mm, which takes no workspace, records its time-outs; looked up
+ * per CUDA context like the no-alloc quantizer's scratch, so make a first
+ * call before any stream capture).  Returns FP8L_OK, FP8L_ETIMEOUT if a
+ * device-side wait of an earlier call gave up (that call's outputs are then
+ * undefined; the workspace's barrier words are zeroed as well, so the next
+ * call starts clean), or FP8L_ECUDA. */
 FP8L_API int fp8l_read_status(void *workspace, void *stream);
 
 /* Testing hook for the bounded device-side waits (this library's failure

@@ -115,6 +115,19 @@ def test_scaled_mm_kernel_choice(lib):
         assert k(1024, 4096, 4096, name) == name
 
 
+def test_w8a16_mm_kernel_choice(lib):
+    import fp8_quantized_linear_gb300 as fl
+    k = fl.w8a16_mm_kernel
+    assert k(1, 4096, 4096) == "stream"
+    assert k(8, 22016, 4096) == "stream"
+    assert k(16, 12288, 4096) == "stream"
+    assert k(17, 4096, 4096) == "swapped"
+    assert k(64, 4096, 11008) == "swapped"
+    assert k(65, 4096, 4096) == "stream"
+    assert k(16, 4096, 4096, "stream") == "stream"
+    assert k(1, 4096, 4096, "swapped") == "swapped"
+
+
 def test_w8a16_argument_errors(lib):
     import fp8_quantized_linear_gb300._binding as b
     f = lib.fp8_w8a16_mm
@@ -127,6 +140,8 @@ def test_w8a16_argument_errors(lib):
     assert f(A16 + 2, b.F16, A16, A16, 1, 32, 32, A16, 0, None) == b.EALIGN
     assert f(A16, b.F16, A16, A16, 1, 32, 32, A16, 4, None) == b.EINVAL
     assert f(A16, b.F16, A16, A16, 1, 32, 32, A16, b.WEIGHTS_PACKED | 8, None) == b.EINVAL
+    assert f(A16, b.F16, A16, A16, 1, 32, 32, A16, b.KERNELS["tiled"], None) == b.EINVAL
+    assert f(A16, b.F16, A16, A16, 65, 32, 32, A16, b.KERNELS["swapped"], None) == b.ESHAPE
 
 
 def test_packed_weight_bytes_and_pack_argument_errors(lib):

@@ -20,11 +20,11 @@ def _no_device_wait_gave_up():
     assert_status_ok()
 
 
-def _w8a16_case(M, N, K, xdtype, seed):
+def _w8a16_case(M, N, K, xdtype, seed, kernel="stream"):
     x = synthetic.activation(M, K, xdtype, seed=seed)
     w = synthetic.weight(N, K, torch.bfloat16, seed=seed)
     qw, sw = oracle.quant_per_row(w)
-    y = fl.fp8_w8a16_mm(dev(x), dev(qw), dev(sw))
+    y = fl.fp8_w8a16_mm(dev(x), dev(qw), dev(sw), kernel=kernel)
     assert y.dtype == xdtype
     return host(y), oracle.w8a16_ref(x, qw, sw)
 
@@ -38,10 +38,11 @@ def test_w8a16_small(M, N, K, xdtype):
 
 
 @pytest.mark.parametrize("shape_idx", range(12))
-def test_w8a16_decode_workload(shape_idx):
+@pytest.mark.parametrize("kernel", ["stream", "auto"])
+def test_w8a16_decode_workload(shape_idx, kernel):
     wl = synthetic.WORKLOADS["decode_w8a16"]
     M, N, K = wl.shapes[shape_idx]
-    y, y_ref = _w8a16_case(M, N, K, torch.float16, seed=wl.seed(shape_idx))
+    y, y_ref = _w8a16_case(M, N, K, torch.float16, seed=wl.seed(shape_idx), kernel=kernel)
     assert_gemm_close(y, y_ref, (M, N, K))
 
 

@@ -56,6 +56,27 @@ def test_product_wait_times_out_then_recovers(M, kernel):
     assert_gemm_close(host(y), y_ref, "after a time-out")
 
 
+def test_w8a16_tensor_core_wait_times_out_then_recovers():
+    # fp8_w8a16_mm takes no workspace: its tensor-core kernel records the
+    # time-out in the library's status word, which fp8l_read_status reports
+    # and clears with the workspace's
+    M, N, K = 16, 512, 1024
+    x = synthetic.activation(M, K, torch.float16, seed=913)
+    qw, sw = oracle.quant_per_row(synthetic.weight(N, K, torch.bfloat16, seed=914))
+    xd, wd, sd = x.to(DEV), torch.from_numpy(qw).to(DEV), torch.from_numpy(sw).to(DEV)
+    ws = fl.workspace(DEV)
+    assert fl.fp8l_read_status(ws) == fl._binding.OK
+    fl.fp8l_debug_waits(SHORT, fl._binding.STALL_MMA)
+    fl.fp8_w8a16_mm(xd, wd, sd, kernel="swapped")
+    torch.cuda.synchronize()
+    assert fl.fp8l_read_status(ws) == fl._binding.ETIMEOUT
+    assert fl.fp8l_read_status(ws) == fl._binding.OK  # reported once, then cleared
+    fl.fp8l_debug_waits(0, 0)
+    y = fl.fp8_w8a16_mm(xd, wd, sd, kernel="swapped")
+    assert fl.fp8l_read_status(ws) == fl._binding.OK
+    assert_gemm_close(host(y), oracle.w8a16_ref(x, qw, sw), "after a time-out")
+
+
 def test_quantizer_grid_barrier_times_out_then_recovers():
     x = synthetic.activation(1024, 4096, torch.bfloat16, seed=907, outlier_frac=0.01)
     q_o, s_o = oracle.quant_per_tensor(x)
