@@ -17,13 +17,14 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfp8linear.so")
 
-ABI_VERSION = 4  # the library version this binding is written for
+ABI_VERSION = 5  # the library version this binding is written for
 F16, BF16, E4M3, F32 = 0, 1, 2, 3
 WEIGHTS_STABLE = 1
 WEIGHTS_PACKED = 2
 A_PER_TOKEN = 4
 SINGLE_SM_TILES = 8
 KERNELS = {"auto": 0, "stream": 16, "swapped": 32, "tiled": 48}  # FP8L_KERNEL_*
+FUSED_DYNAMIC_MAX_BYTES = 65536  # FP8L_FUSED_DYNAMIC_MAX_BYTES
 OK, EINVAL, ESHAPE, EALIGN, ECUDA, ETIMEOUT, EUNSUPPORTED = range(7)
 
 _DTYPE_CODE = {torch.float16: F16, torch.bfloat16: BF16, torch.float32: F32,
@@ -74,6 +75,9 @@ def load():
         lib.fp8_quant_per_row.argtypes = [P, I, I64, I64, P, P, P]
         lib.fp8_scaled_mm.restype = I
         lib.fp8_scaled_mm.argtypes = [P, P, I64, I64, I64, P, P, I, P, P, I, P, ctypes.c_uint, P]
+        lib.fp8_quant_scaled_mm.restype = I
+        lib.fp8_quant_scaled_mm.argtypes = [P, I, P, I64, I64, I64, P, I, P, I, P, P, I, P,
+                                            ctypes.c_uint, P]
         lib.fp8_w8a16_mm_kernel.restype = ctypes.c_uint
         lib.fp8_w8a16_mm_kernel.argtypes = [I64, I64, I64, ctypes.c_uint]
         lib.fp8_scaled_mm_kernel.restype = ctypes.c_uint
@@ -239,6 +243,45 @@ def scaled_mm_kernel(M: int, N: int, K: int, kernel: str = "auto") -> str:
     for this shape and kernel choice (fp8_scaled_mm_kernel; no GPU needed)."""
     code = load().fp8_scaled_mm_kernel(M, N, K, KERNELS[kernel])
     return {v: k for k, v in KERNELS.items()}[code]
+
+
+def fp8_quant_scaled_mm(x: torch.Tensor, w: torch.Tensor, w_scale: torch.Tensor,
+                        a_scale: torch.Tensor | None = None, dynamic: bool = True,
+                        out_dtype=torch.bfloat16, out_scale: torch.Tensor | None = None,
+                        y: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                        stable_weights: bool = False):
+    """W8A8 product of 16-bit x [M <= 128, K] and E4M3 w [N, K] with the
+    per-tensor activation quantization fused into it (fp8_quant_scaled_mm):
+    dynamic writes a_scale (a new [1] tensor when None), static reads it.
+    Returns (y, a_scale)."""
+    _need_cuda(x, w, w_scale, a_scale, out_scale, y, ws)
+    w = _codes(w)
+    M, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K:
+        raise ValueError("inner dimensions differ")
+    if a_scale is None:
+        if not dynamic:
+            raise ValueError("a static scale must be given")
+        a_scale = torch.empty(1, dtype=torch.float32, device=x.device)
+    if out_dtype == torch.float8_e4m3fn:
+        out_dtype = torch.uint8
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    if ws is None:
+        ws = workspace(x.device)
+    if w_scale.numel() not in (1, N):
+        raise ValueError("w_scale must have 1 or N entries")
+    per_channel = 1 if w_scale.numel() == N and N != 1 else 0
+    with torch.cuda.device(x.device):
+        st = load().fp8_quant_scaled_mm(
+            x.data_ptr(), _DTYPE_CODE[x.dtype], w.data_ptr(), M, N, K, a_scale.data_ptr(),
+            1 if dynamic else 0, w_scale.data_ptr(), per_channel,
+            out_scale.data_ptr() if out_scale is not None else None, _codes(y).data_ptr(),
+            _DTYPE_CODE[y.dtype], ws.data_ptr(), WEIGHTS_STABLE if stable_weights else 0,
+            _stream(x.device))
+    _check(st, "fp8_quant_scaled_mm")
+    return y, a_scale
 
 
 def w8a16_mm_kernel(M: int, N: int, K: int, kernel: str = "auto") -> str:

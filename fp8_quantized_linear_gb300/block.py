@@ -18,9 +18,12 @@ each product's input a function of the previous output).
   * "w8a16": fp16 activations times E4M3 weights with per-channel scales
     (fp8_w8a16_mm), the decode path; weights packed at set-up.
   * "w8a8": bf16 activations; RMSNorm fused with the dynamic per-tensor
-    quantization before q/k/v (fp8_rmsnorm_quant), the separate dynamic
-    quantizer before o, gate/up and down (fp8_quant_per_tensor), the W8A8
-    product (fp8_scaled_mm) with per-channel weight scales, bf16 outputs.
+    quantization before q/k/v (fp8_rmsnorm_quant) and the W8A8 product
+    (fp8_scaled_mm) with per-channel weight scales, bf16 outputs; before o,
+    gate/up and down the dynamic quantization runs inside the product
+    (fp8_quant_scaled_mm) when the activations are small enough for every
+    CTA to read them (a few tokens), else as its own launch
+    (fp8_quant_per_tensor).
 
 Every call goes through the binding to the library's kernels; this module
 only owns the buffers and the order of the calls.
@@ -89,6 +92,11 @@ class DecodeBlock:
             if name == "qkv":
                 b.fp8_rmsnorm_quant(inp, self.gamma, self.eps, q=self.qa[name],
                                     scale=self.sa[name], ws=self.ws)
+            elif self.fused(name):
+                b.fp8_quant_scaled_mm(inp, self.w[name], self.sw[name], a_scale=self.sa[name],
+                                      dynamic=True, out_dtype=self.act_dtype, y=self.y[name],
+                                      ws=self.ws, stable_weights=True)
+                continue
             else:
                 b.fp8_quant_per_tensor(inp, q=self.qa[name], scale=self.sa[name], ws=self.ws)
             b.fp8_scaled_mm(self.qa[name], self.w[name], self.sa[name], self.sw[name],
@@ -96,9 +104,18 @@ class DecodeBlock:
                             stable_weights=True)
         return self.y["down"]
 
+    def fused(self, name: str) -> bool:
+        """Whether the product `name` runs with its quantization fused (W8A8,
+        not q/k/v, activations within FUSED_DYNAMIC_MAX_BYTES)."""
+        K = SHAPES[name][1]
+        return (self.kind == "w8a8" and name != "qkv" and
+                2 * self.M * K <= b.FUSED_DYNAMIC_MAX_BYTES)
+
     def launches(self) -> int:
         """Kernel launches of one forward()."""
-        return 4 if self.kind == "w8a16" else 8
+        if self.kind == "w8a16":
+            return 4
+        return sum(1 if self.fused(n) else 2 for n in ORDER)
 
     def capture(self, stream: torch.cuda.Stream | None = None) -> torch.cuda.CUDAGraph:
         """Runs forward() once eagerly (library set-up outside the capture),

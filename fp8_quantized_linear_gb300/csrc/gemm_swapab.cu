@@ -42,6 +42,7 @@
 
 #include <atomic>
 
+#include "quant_device.cuh"
 #include "tc_device.cuh"
 
 namespace fp8l {
@@ -67,6 +68,7 @@ struct SwapParams {
     int num_k_blocks;
     int split;        // CTAs of a cluster sharing a tile (1: no cluster)
     int prefetch;     // stable weights: weight blocks issued before griddepcontrol.wait
+    int x_stages;     // fused quantization: stages of the 16-bit token ring
     const float *a_scale;
     const float *w_scale;
     int w_per_channel;
@@ -108,6 +110,15 @@ __device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
     float4 v;
     asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4u(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(addr)
                  : "memory");
     return v;
@@ -303,8 +314,8 @@ gemm_f8_swapab(const __grid_constant__ CUtensorMap tmap_w,
         for (int j = 0; j < 4; ++j) v[j] *= sa * (p.w_per_channel ? ld_f32(p.w_scale + n + j) : sw0);
         const size_t o = static_cast<size_t>(t) * p.N + n;
         if (p.out_dtype == FP8L_E4M3) {
-            const uint32_t lo = e4m3x2(od.quot(v[0]), od.quot(v[1]));
-            const uint32_t hi = e4m3x2(od.quot(v[2]), od.quot(v[3]));
+            const uint32_t lo = out_e4m3x2(od.quot(v[0]), od.quot(v[1]));
+            const uint32_t hi = out_e4m3x2(od.quot(v[2]), od.quot(v[3]));
             *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(p.y) + o) = lo | (hi << 16);
         } else {
             *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.y) + o) =
@@ -312,6 +323,342 @@ gemm_f8_swapab(const __grid_constant__ CUtensorMap tmap_w,
         }
     }
     if (split > 1) cluster_sync_all();  // peers may still be reading this CTA's partials
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(tmem_cols)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- with the quantization fused
+//
+// The same product with the activations' E4M3 codes made inside the kernel
+// from 16-bit x ("Condition to achieve linear speedup?": activation
+// quantization fused into another kernel; "RFC: FP8 Quantization Schema in
+// vLLM": static input scales), so no quantizer launch precedes it:
+//   static scale    a_scale given; each CTA quantizes only the token
+//                   columns of its own k-blocks;
+//   dynamic scale   every CTA first takes the magnitude maximum of the whole
+//                   x (a few to a few tens of KB for a few tokens; read from
+//                   L2) and derives the same scale = amax / 448; CTA 0 stores
+//                   it in a_scale.
+// The codes are those of the quantizer bit for bit (the same division-free
+// quotient and E4M3 conversion), so the result equals quantizer + product.
+//   warp 0      lane 0: weight stages (as above).
+//   warp 1      TMEM; lane 0 issues the MMAs once a stage's weights have
+//               landed and its token codes are written.
+//   warps 2-3   converters: the codes of the M token rows of each k-block,
+//               16 per thread and step, into the stage's swizzled B tile
+//               (rows M .. T-1 stay zero), then a proxy fence.
+//   warp 4      lane 0: the tokens' 16-bit k-blocks (two M x 64 boxes:
+//               only the real token rows) into a ring of up to 16 stages
+//               (24 KB).
+// Every weight stage and token stage has one consumer in k-block order (no
+// barrier can be waited on two phases ahead).
+// Token ring: as many stages as fit kSqXRingBytes, 2 to kSqMaxXStages (with
+// two stages a CTA streaming 32 k-blocks waited on its token loads: 34 us
+// against 25 us for quantizer + product at M = 1, N = 28672).  Above 64
+// tokens the ring takes the shared memory past two CTAs per SM: one CTA per
+// SM then, up to kSqSmemMax.
+constexpr int kSqMaxXStages = 16;
+constexpr size_t kSqXRingBytes = 24 * 1024;
+constexpr size_t kSqSmemMax = 220 * 1024;
+constexpr int kSqConvThreads = 64;
+// warp 4 loads the tokens: in lane 1 of the weight producer's warp its
+// spin-waits and the weight producer's took turns (N = 28672 at M = 1:
+// 32 us against 25 us for quantizer + product)
+constexpr int kSqThreads = 160;
+
+template <int XDT>
+__global__ void __launch_bounds__(kSqThreads, 1)
+gemm_f8_swapab_q(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
+                 const SwapParams p, float *a_scale_out, int dynamic, const void *x_raw) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (sbase - raw);
+    const int S = p.stages, SX = p.x_stages;
+    const uint32_t sb = static_cast<uint32_t>(p.stage_bytes);   // 16 KB of weights + T x 128 codes
+    const uint32_t xsb = static_cast<uint32_t>(p.M) * 256u;      // M rows x 128 16-bit values
+    const uint32_t xbase = sbase + static_cast<uint32_t>(S) * sb;
+    const uint32_t ring_bytes = static_cast<uint32_t>(S) * sb + static_cast<uint32_t>(SX) * xsb;
+    const uint32_t bar0 = (sbase + ring_bytes + 7u) & ~7u;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+    auto bready_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
+    auto xfull_bar = [&](int s) { return bar0 + 8u * (3 * S + s); };
+    auto xempty_bar = [&](int s) { return bar0 + 8u * (3 * S + SX + s); };
+    const uint32_t done_bar = bar0 + 8u * (3 * S + 2 * SX);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + (bar0 - sbase) + (3 * S + 2 * SX + 1) * 8);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    __shared__ uint32_t red[33];
+    const uint32_t tmem_cols = p.T <= 32 ? 32u : (p.T <= 64 ? 64u : 128u);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int split = p.split;
+    const int rank = split > 1 ? static_cast<int>(blockIdx.x) % split : 0;
+    const int tile = static_cast<int>(blockIdx.x) / split;
+    const int base = p.num_k_blocks / split, rem = p.num_k_blocks % split;
+    const int kb_begin = rank * base + (rank < rem ? rank : rem);
+    const int nkb = base + (rank < rem ? 1 : 0);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+            mbar_init(bready_bar(s), kSqConvThreads);
+        }
+        for (int s = 0; s < SX; ++s) {
+            mbar_init(xfull_bar(s), 1);
+            mbar_init(xempty_bar(s), kSqConvThreads);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    // stable weights: the first stages' weight blocks before the wait
+    const int pre = p.prefetch ? (nkb < S ? nkb : S) : 0;
+    if (warp == 0 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_x)) : "memory");
+        for (int i = 0; i < pre; ++i) {
+            mbar_expect_tx(full_bar(i), kSwWBytes);
+            tma_load_2d(sbase + i * sb, &tmap_w, (kb_begin + i) * SW_BK, tile * SW_BM, full_bar(i));
+        }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // the activation scale: given, or the dynamic one from the whole of x
+    float sa;
+    if (dynamic) {
+        const uint4 *xv = static_cast<const uint4 *>(x_raw);
+        const int64_t words = static_cast<int64_t>(p.M) * p.K / 8;  // 8 16-bit values per word
+        // eight loads in flight per thread before any is used: a few tens of
+        // KB are then read in one or two L2 round trips
+        uint32_t m = 0;
+        for (int64_t w0 = threadIdx.x; w0 < words; w0 += 8 * kSqThreads) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int64_t w = w0 + static_cast<int64_t>(u) * kSqThreads;
+                v[u] = make_uint4(0, 0, 0, 0);
+                if (w < words)
+                    asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(v[u].x), "=r"(v[u].y), "=r"(v[u].z), "=r"(v[u].w)
+                                 : "l"(xv + w));
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) m = word_mag_max<XDT>(v[u], m);
+        }
+        m = block_max_u32(fold_mag<XDT>(m), red);
+        sa = scale_from_amax(mag_bits_to_float<XDT>(m));
+        if (blockIdx.x == 0 && threadIdx.x == 0) *a_scale_out = sa;
+    } else {
+        sa = ld_f32(a_scale_out);
+    }
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const int w_row = tile * SW_BM;
+            uint32_t issued = (1u << pre) - 1u;
+            uint32_t issued_parity = 0;
+            int stage = pre == S ? 0 : pre;
+            uint32_t phase = pre == S ? 1u : 0u;
+            for (int i = pre; i < nkb; ++i) {
+                if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.wait_cycles)) break;
+                mbar_expect_tx(full_bar(stage), kSwWBytes);
+                tma_load_2d(sbase + stage * sb, &tmap_w, (kb_begin + i) * SW_BK, w_row, full_bar(stage));
+                issued |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            for (int s = 0; s < S; ++s)
+                if (issued & (1u << s)) mbar_wait_drain(full_bar(s), (issued_parity >> s) & 1u, p.status);
+        }
+        __syncwarp();
+    } else if (warp == 4) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, issued_parity = 0;
+            for (int i = 0; i < nkb; ++i) {
+                if (!mbar_wait(xempty_bar(stage), phase ^ 1u, abort_flag, p.status, p.wait_cycles)) break;
+                const uint32_t dst = xbase + static_cast<uint32_t>(stage) * xsb;
+                const int kx = (kb_begin + i) * SW_BK;
+                mbar_expect_tx(xfull_bar(stage), xsb);
+                tma_load_2d(dst, &tmap_x, kx, 0, xfull_bar(stage));
+                tma_load_2d(dst + xsb / 2, &tmap_x, kx + 64, 0, xfull_bar(stage));
+                issued |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == SX) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            for (int s = 0; s < SX; ++s)
+                if (issued & (1u << s)) mbar_wait_drain(xfull_bar(s), (issued_parity >> s) & 1u, p.status);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = (1u << 4) | (static_cast<uint32_t>(p.T >> 3) << 17) |
+                                   (static_cast<uint32_t>(SW_BM >> 4) << 24);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            if (p.stall & kStallMma) ok = mbar_wait(done_bar, 0, abort_flag, p.status, p.wait_cycles);
+            for (int i = 0; ok && i < nkb; ++i) {
+                if (!mbar_wait_fast(full_bar(stage), phase, abort_flag, p.status, p.wait_cycles) ||
+                    !mbar_wait_fast(bready_bar(stage), phase, abort_flag, p.status, p.wait_cycles))
+                    break;
+                tc_fence_after();
+                const uint32_t st = sbase + stage * sb;
+                const uint64_t dw = sw128_desc(st), da = sw128_desc(st + kSwWBytes);
+#pragma unroll
+                for (int k = 0; k < SW_BK / SW_UMMA_K; ++k)
+                    mma_f8_n(tmem_base, dw + 2 * k, da + 2 * k, idesc, (i | k) != 0 ? 1u : 0u);
+                mma_commit(empty_bar(stage));
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            mma_commit(done_bar);
+        }
+        __syncwarp();
+    } else {
+        // converters: rows M .. T-1 of every stage's code tile are zero once
+        const int ct = static_cast<int>(threadIdx.x) - 64;
+        for (int s = 0; s < S; ++s)
+            for (int o = ct * 16 + p.M * 128; o < p.T * 128; o += kSqConvThreads * 16)
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sbase + s * sb + kSwWBytes +
+                                                                             static_cast<uint32_t>(o)),
+                             "r"(0u)
+                             : "memory");
+        const Quot d = Quot::make<XDT>(sa);
+        int stage = 0, xs = 0;
+        uint32_t phase = 0, xphase = 0;
+        for (int i = 0; i < nkb; ++i) {
+            // the token block has landed, and the stage's code tile is free
+            // (the MMAs of its previous round have retired)
+            if (!mbar_wait(xfull_bar(xs), xphase, abort_flag, p.status, p.wait_cycles) ||
+                !mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.wait_cycles))
+                break;
+            const uint32_t xst = xbase + static_cast<uint32_t>(xs) * xsb;
+            const uint32_t bst = sbase + stage * sb + kSwWBytes;
+            // task (row r, 16-code piece j): x values 16 j .. 16 j + 15 of row r
+            for (int task = ct; task < p.M * 8; task += kSqConvThreads) {
+                const int r = task >> 3, j = task & 7;
+                // the stage holds two M x 64 boxes (k 0-63, 64-127) of 128-byte rows
+                const uint32_t src = xst + static_cast<uint32_t>((j >> 2) * (xsb / 2) + r * 128 + (j & 3) * 32);
+                const uint4 v0 = ld_shared_v4u(src), v1 = ld_shared_v4u(src + 16);
+                const uint2 c0 = dynamic ? codes_of_word<XDT, false>(v0, d) : codes_of_word<XDT, true>(v0, d);
+                const uint2 c1 = dynamic ? codes_of_word<XDT, false>(v1, d) : codes_of_word<XDT, true>(v1, d);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                 bst + static_cast<uint32_t>(r * 128 + ((j ^ (r & 7)) * 16))),
+                             "r"(c0.x), "r"(c0.y), "r"(c1.x), "r"(c1.y)
+                             : "memory");
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // codes visible to the MMAs
+            mbar_arrive(bready_bar(stage));
+            mbar_arrive(xempty_bar(xs));
+            if (++stage == S) {
+                stage = 0;
+                phase ^= 1u;
+            }
+            if (++xs == SX) {
+                xs = 0;
+                xphase ^= 1u;
+            }
+        }
+    }
+
+    // ---- epilogue (as in gemm_f8_swapab, with this CTA's own scale;
+    // warps 0-3 own the TMEM lane quarters)
+    const bool done_ok = mbar_wait(done_bar, 0, abort_flag, p.status, p.wait_cycles);
+    tc_fence_after();
+    const int row = warp * 32 + lane;
+    if (warp < 4 && done_ok && !*abort_flag) {
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
+        for (int c = 0; c < p.T; c += 16) {
+            uint32_t r[16];
+            tmem_ld16(taddr + static_cast<uint32_t>(c), r);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                st_shared_f32(sbase + static_cast<uint32_t>(((c + j) * kSwPitch + row) * 4), r[j]);
+        }
+    }
+    tc_fence_before();
+    if (split > 1)
+        cluster_sync_all();
+    else
+        __syncthreads();
+    const bool ok = !*abort_flag;
+    const int items = p.M * (SW_BM / 4);
+    const int i0 = static_cast<int>((static_cast<long long>(items) * rank) / split);
+    const int i1 = static_cast<int>((static_cast<long long>(items) * (rank + 1)) / split);
+    const float sw0 = ld_f32(p.w_scale);
+    const OutDiv od = OutDiv::make(p.out_dtype == FP8L_E4M3 ? ld_f32(p.out_scale) : 1.0f);
+    for (int i = i0 + static_cast<int>(threadIdx.x); ok && i < i1; i += kSqThreads) {
+        const int t = i >> 5;
+        const int c4 = (i & 31) * 4;
+        const int n = tile * SW_BM + c4;
+        if (n >= p.N) continue;
+        const uint32_t off = sbase + static_cast<uint32_t>((t * kSwPitch + c4) * 4);
+        float4 acc;
+        if (split == 1) {
+            acc = ld_shared_v4(off);
+        } else {
+            float4 part[kSwMaxSplit];
+#pragma unroll
+            for (int q = 0; q < kSwMaxSplit; ++q)
+                if (q < split) part[q] = ld_cluster_v4(off, static_cast<uint32_t>(q));
+            acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < kSwMaxSplit; ++q) {  // the same order in every run
+                if (q < split) {
+                    acc.x += part[q].x;
+                    acc.y += part[q].y;
+                    acc.z += part[q].z;
+                    acc.w += part[q].w;
+                }
+            }
+        }
+        float v[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] *= sa * (p.w_per_channel ? ld_f32(p.w_scale + n + j) : sw0);
+        const size_t o = static_cast<size_t>(t) * p.N + n;
+        if (p.out_dtype == FP8L_E4M3) {
+            const uint32_t lo = out_e4m3x2(od.quot(v[0]), od.quot(v[1]));
+            const uint32_t hi = out_e4m3x2(od.quot(v[2]), od.quot(v[3]));
+            *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(p.y) + o) = lo | (hi << 16);
+        } else {
+            *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.y) + o) =
+                make_uint2(pack_out16(v[0], v[1], p.out_dtype), pack_out16(v[2], v[3], p.out_dtype));
+        }
+    }
+    if (split > 1) cluster_sync_all();
 
     tc_fence_before();
     __syncthreads();
@@ -337,12 +684,12 @@ gemm_f8_swapab(const __grid_constant__ CUtensorMap tmap_w,
 // or zero, and its 3-bit significand fits bf16's 7), done by converter
 // warps, and the widened weights go to TMEM as the MMA's A operand; the
 // tokens are the B operand in shared memory.
-//   warp 0         TMA producers, one lane per ring: lane 0 the weights (per
-//                  128-element k-block, the raw 128 x 128-byte block: rows
-//                  of the [N, K] matrix with the 128-byte swizzle, or 8
-//                  groups x 2 chunks of the packed layout read as 2 KB
-//                  runs), lane 1 the tokens (two T x 64 blocks, 128-byte
-//                  swizzle).
+//   warp 0         weight producer: per 128-element k-block the raw 128 x
+//                  128-byte block (rows of the [N, K] matrix with the
+//                  128-byte swizzle, or 8 groups x 2 chunks of the packed
+//                  layout read as 2 KB runs).
+//   warp 10        token producer: two T x 64 blocks (128-byte swizzle) per
+//                  k-block.
 //   warp 1         TMEM (256 columns: two 64-column A buffers, then the
 //                  T <= 64 accumulator columns); lane 0 issues
 //                  tcgen05.mma.cta_group::1.kind::f16 [d], [a], b (M = 128,
@@ -368,7 +715,8 @@ gemm_f8_swapab(const __grid_constant__ CUtensorMap tmap_w,
 constexpr int W16_BK = 128;                    // k-block, elements
 constexpr int W16_UMMA_K = 16;                 // K of one kind::f16 MMA
 constexpr int kW16Groups = 2;                  // converter warpgroups, alternate k-blocks
-constexpr int kW16Threads = 64 + 128 * kW16Groups;
+constexpr int kW16XWarp = 2 + 4 * kW16Groups;  // the token producer's own warp
+constexpr int kW16Threads = 32 * (kW16XWarp + 1);
 constexpr int kW16WBytes = SW_BM * W16_BK;     // 16 KB of E4M3 weights per stage
 constexpr int kW16MaxT = 64;
 constexpr int kW16ABufCols = W16_BK / 2;       // two 16-bit values per TMEM column
@@ -384,7 +732,6 @@ constexpr uint32_t kW16TmemCols = 256;
 constexpr int kW16ConvThreads = 128;
 constexpr int kW16MaxWStages = 8;
 static_assert(kW16MaxWStages % kW16Groups == 0, "weight stages are dealt to the converter groups");
-constexpr int kW16MaxXStages = 8;
 
 struct W16Params {
     int M, N, K;
@@ -459,7 +806,7 @@ __device__ __forceinline__ uint32_t f16x2_to_bf16x2_e4m3(uint32_t h) {
 
 // 16 E4M3 codes to 8 words of 16-bit pairs of x's type
 template <int XDT>
-__device__ __forceinline__ void widen16(const uint4 &u, uint32_t *h) {
+__device__ __forceinline__ void widen_codes16(const uint4 &u, uint32_t *h) {
     const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -563,7 +910,10 @@ gemm_w8a16_tc(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant_
             }
             for (int s = 0; s < SW; ++s)
                 if (issued & (1u << s)) mbar_wait_drain(wfull_bar(s), (issued_parity >> s) & 1u, p.status);
-        } else if (lane == 1) {
+        }
+        __syncwarp();
+    } else if (warp == kW16XWarp) {
+        if (lane == 0) {
             // tokens: written by the preceding kernel
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_x)) : "memory");
             asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -677,7 +1027,7 @@ gemm_w8a16_tc(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant_
                         u = src == 2 ? v[4 * half + 2] : u;
                         u = src == 3 ? v[4 * half + 3] : u;
                     }
-                    widen16<XDT>(u, h + 8 * c);
+                    widen_codes16<XDT>(u, h + 8 * c);
                 }
                 tmem_st32(tmem_base + lane_addr + static_cast<uint32_t>(buf * kW16ABufCols + 32 * half), h);
             }
@@ -792,6 +1142,14 @@ int ensure_attr(int dev) {
                              static_cast<int>(kSwSmemMax)) != cudaSuccess ||
         cudaFuncSetAttribute(gemm_f8_swapab, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_f8_swapab_q<FP8L_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSqSmemMax)) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_f8_swapab_q<FP8L_F16>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_f8_swapab_q<FP8L_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSqSmemMax)) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_f8_swapab_q<FP8L_BF16>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
         cudaFuncSetAttribute(gemm_w8a16_tc<FP8L_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSwSmemMax)) != cudaSuccess ||
         cudaFuncSetAttribute(gemm_w8a16_tc<FP8L_F16>, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -801,8 +1159,12 @@ int ensure_attr(int dev) {
         cudaFuncSetAttribute(gemm_w8a16_tc<FP8L_BF16>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
         cudaFuncSetAttribute(swapab_occupancy_twin<kSwThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSwSmemMax)) != cudaSuccess ||
+                             static_cast<int>(kSqSmemMax)) != cudaSuccess ||
         cudaFuncSetAttribute(swapab_occupancy_twin<kSwThreads>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+        cudaFuncSetAttribute(swapab_occupancy_twin<kSqThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSqSmemMax)) != cudaSuccess ||
+        cudaFuncSetAttribute(swapab_occupancy_twin<kSqThreads>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
         cudaFuncSetAttribute(swapab_occupancy_twin<kW16Threads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSwSmemMax)) != cudaSuccess ||
@@ -819,9 +1181,9 @@ int ensure_attr(int dev) {
 
 // Clusters of `split` CTAs of this block size and ring size that the GPU
 // holds at once (cudaOccupancyMaxActiveClusters of the twin kernel: clusters
-// sit within one GPC), cached per device, kernel (0: W8A8, 1: W8A16), token
-// tile and split.
-std::atomic<int> g_max_clusters[kMaxDevices][2][kSwMaxT / 16][kSwMaxSplit + 1];
+// sit within one GPC), cached per device, kernel (0: W8A8, 1: W8A16, 2: W8A8
+// with the quantization fused), token tile and split.
+std::atomic<int> g_max_clusters[kMaxDevices][3][kSwMaxT / 16][kSwMaxSplit + 1];
 
 int max_clusters(int dev, int kernel, int T, size_t smem, int split) {
     std::atomic<int> &slot = g_max_clusters[dev][kernel][T / 16 - 1][split];
@@ -829,7 +1191,7 @@ int max_clusters(int dev, int kernel, int T, size_t smem, int split) {
     if (n > 0) return n;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(split), 1, 1);
-    cfg.blockDim = dim3(kernel == 0 ? kSwThreads : kW16Threads, 1, 1);
+    cfg.blockDim = dim3(kernel == 1 ? kW16Threads : (kernel == 2 ? kSqThreads : kSwThreads), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -838,9 +1200,10 @@ int max_clusters(int dev, int kernel, int T, size_t smem, int split) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = kernel == 0
-                              ? cudaOccupancyMaxActiveClusters(&n, swapab_occupancy_twin<kSwThreads>, &cfg)
-                              : cudaOccupancyMaxActiveClusters(&n, swapab_occupancy_twin<kW16Threads>, &cfg);
+    const cudaError_t e =
+        kernel == 1   ? cudaOccupancyMaxActiveClusters(&n, swapab_occupancy_twin<kW16Threads>, &cfg)
+        : kernel == 2 ? cudaOccupancyMaxActiveClusters(&n, swapab_occupancy_twin<kSqThreads>, &cfg)
+                      : cudaOccupancyMaxActiveClusters(&n, swapab_occupancy_twin<kSwThreads>, &cfg);
     if (e != cudaSuccess || n < 1) {
         (void)cudaGetLastError();
         n = 1;
@@ -902,6 +1265,7 @@ int launch_swapab(const uint8_t *a, const uint8_t *w, int M, int N, int K, const
     p.wait_cycles = wc.cycles;
     p.stall = wc.stall;
     p.prefetch = stable ? 1 : 0;
+    p.x_stages = 0;
 
     // split: the largest cluster whose launch runs in one wave (a cluster
     // sits in one GPC, so fewer clusters of s CTAs fit than slots / s: at
@@ -1030,4 +1394,117 @@ int launch_w8a16_tc(const void *x, int x_dtype, const uint8_t *w, bool packed, c
     return launch_status();
 }
 
+// Swapped-operand product with the activation quantization fused
+// (fp8_quant_scaled_mm): 1 <= M <= 128, dynamic mode up to
+// FP8L_FUSED_DYNAMIC_MAX_BYTES of x.  Weight stages as in launch_swapab, less
+// the two 16-bit token stages.
+int launch_swapab_q(const void *x, int x_dtype, const uint8_t *w, int M, int N, int K, float *a_scale,
+                    int dynamic, const float *w_scale, int w_per_channel, const float *out_scale, void *y,
+                    int out_dtype, unsigned *status, int sms, bool stable, cudaStream_t stream) {
+    if (M < 1 || M > kSwMaxT) return FP8L_ESHAPE;
+    if (dynamic && int64_t(M) * K * 2 > FP8L_FUSED_DYNAMIC_MAX_BYTES) return FP8L_ESHAPE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP8L_ECUDA;
+    if (ensure_attr(dev) != FP8L_OK) return FP8L_ECUDA;
+    SwapParams p;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.T = (M + 15) & ~15;
+    p.stage_bytes = kSwWBytes + p.T * SW_BK;
+    const size_t xsb = size_t(M) * 256;
+    int xst = static_cast<int>(kSqXRingBytes / xsb);
+    if (xst > kSqMaxXStages) xst = kSqMaxXStages;
+    if (xst < 2) xst = 2;
+    p.x_stages = xst;
+    const size_t xring = size_t(xst) * xsb;
+    int stages = static_cast<int>((size_t(kSwSmemTarget) - 1024 - 64 - 16 * xst - xring) / (p.stage_bytes + 24));
+    if (stages > kSwMaxStages) stages = kSwMaxStages;
+    if (stages < 3) stages = 3;
+    p.stages = stages;
+    const size_t ring = size_t(stages) * p.stage_bytes + xring;
+    const size_t smem = 1024 + ((ring + 7) & ~size_t(7)) + size_t(3 * stages + 2 * xst + 1) * 8 + 16;
+    if (smem > kSqSmemMax || size_t(p.T) * kSwPitch * 4 > size_t(stages) * p.stage_bytes)
+        return FP8L_ESHAPE;
+    p.num_k_blocks = (K + SW_BK - 1) / SW_BK;
+    p.a_scale = a_scale;
+    p.w_scale = w_scale;
+    p.w_per_channel = w_per_channel;
+    p.a_per_token = 0;
+    p.out_scale = out_scale;
+    p.y = y;
+    p.out_dtype = out_dtype;
+    p.status = status;
+    const WaitConfig wc = wait_config();
+    p.wait_cycles = wc.cycles;
+    p.stall = wc.stall;
+    p.prefetch = stable ? 1 : 0;
+    const int tiles = (N + SW_BM - 1) / SW_BM;
+    p.split = pick_split(dev, 2, p.T, smem, tiles, p.num_k_blocks, sms);
+
+    CUtensorMap mw, mx;
+    if (make_kmajor_map(&mw, w, N, K, SW_BK, SW_BM) != FP8L_OK) return FP8L_ECUDA;
+    {
+        const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
+        const uint64_t strides[1] = {static_cast<uint64_t>(K) * 2};
+        const uint32_t box[2] = {64, static_cast<uint32_t>(M)};
+        if (make_tile_map(&mx, x, 2, 2, dims, strides, box, false) != FP8L_OK) return FP8L_ECUDA;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(int64_t(tiles) * p.split), 1, 1);
+    cfg.blockDim = dim3(kSqThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int nattr = 0;
+    if (p.split > 1) {
+        attr[nattr].id = cudaLaunchAttributeClusterDimension;
+        attr[nattr].val.clusterDim.x = static_cast<unsigned>(p.split);
+        attr[nattr].val.clusterDim.y = 1;
+        attr[nattr].val.clusterDim.z = 1;
+        ++nattr;
+    }
+    if (stable) {
+        attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+        ++nattr;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = nattr;
+    const cudaError_t e =
+        x_dtype == FP8L_BF16
+            ? cudaLaunchKernelEx(&cfg, gemm_f8_swapab_q<FP8L_BF16>, mw, mx, p, a_scale, dynamic, x)
+            : cudaLaunchKernelEx(&cfg, gemm_f8_swapab_q<FP8L_F16>, mw, mx, p, a_scale, dynamic, x);
+    if (e != cudaSuccess) return FP8L_ECUDA;
+    return launch_status();
+}
+
 }  // namespace fp8l
+
+extern "C" int fp8_quant_scaled_mm(const void *x, int x_dtype, const uint8_t *w, int64_t M, int64_t N,
+                                   int64_t K, float *a_scale, int dynamic, const float *w_scale,
+                                   int w_per_channel, const float *out_scale, void *y, int out_dtype,
+                                   void *workspace, unsigned flags, void *stream) {
+    using namespace fp8l;
+    if (x_dtype != FP8L_F16 && x_dtype != FP8L_BF16) return FP8L_EINVAL;
+    if (out_dtype != FP8L_F16 && out_dtype != FP8L_BF16 && out_dtype != FP8L_E4M3) return FP8L_EINVAL;
+    if ((flags & ~FP8L_WEIGHTS_STABLE) != 0u) return FP8L_EINVAL;
+    if (a_scale == nullptr || w_scale == nullptr || workspace == nullptr || w == nullptr) return FP8L_EINVAL;
+    if (out_dtype == FP8L_E4M3 && out_scale == nullptr) return FP8L_EINVAL;
+    if (M < 0 || M > 128 || N <= 0 || K <= 0 || N > (1 << 20) || K > (1 << 20) || N % 16 != 0 ||
+        K % 16 != 0)
+        return FP8L_ESHAPE;
+    if (dynamic && M * K * 2 > FP8L_FUSED_DYNAMIC_MAX_BYTES) return FP8L_ESHAPE;
+    if (M > 0 && (x == nullptr || y == nullptr)) return FP8L_EINVAL;
+    auto misaligned4 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) != 0; };
+    if (!aligned16(w) || !aligned16(workspace) || (M > 0 && (!aligned16(x) || !aligned16(y))) ||
+        misaligned4(a_scale) || misaligned4(w_scale) || (out_dtype == FP8L_E4M3 && misaligned4(out_scale)))
+        return FP8L_EALIGN;
+    int sms = 0;
+    int st = check_device(&sms);
+    if (st != FP8L_OK) return st;
+    if (M == 0) return FP8L_OK;
+    return launch_swapab_q(x, x_dtype, w, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                           a_scale, dynamic ? 1 : 0, w_scale, w_per_channel ? 1 : 0, out_scale, y, out_dtype,
+                           status_word(workspace), sms, (flags & FP8L_WEIGHTS_STABLE) != 0u, as_stream(stream));
+}

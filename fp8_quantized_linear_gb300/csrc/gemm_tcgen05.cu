@@ -121,8 +121,8 @@ __device__ __forceinline__ void store_row_chunk(const GemmParams &p, const uint3
         uint32_t w[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const uint32_t lo = e4m3x2(d.quot(v[4 * i]), d.quot(v[4 * i + 1]));
-            const uint32_t hi = e4m3x2(d.quot(v[4 * i + 2]), d.quot(v[4 * i + 3]));
+            const uint32_t lo = out_e4m3x2(d.quot(v[4 * i]), d.quot(v[4 * i + 1]));
+            const uint32_t hi = out_e4m3x2(d.quot(v[4 * i + 2]), d.quot(v[4 * i + 3]));
             w[i] = lo | (hi << 16);
         }
         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.y) +
@@ -230,8 +230,8 @@ __device__ void split_reduce_store(const GemmParams &p, int tile, int rank, uint
             v[j] *= sa * (p.w_per_channel ? __ldg(p.w_scale + n + j) : sw0);
         if (p.out_dtype == FP8L_E4M3) {
             const OutDiv d = OutDiv::make(__ldg(p.out_scale));
-            const uint32_t lo = e4m3x2(d.quot(v[0]), d.quot(v[1]));
-            const uint32_t hi = e4m3x2(d.quot(v[2]), d.quot(v[3]));
+            const uint32_t lo = out_e4m3x2(d.quot(v[0]), d.quot(v[1]));
+            const uint32_t hi = out_e4m3x2(d.quot(v[2]), d.quot(v[3]));
             *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(p.y) + static_cast<size_t>(m) * p.N + n) =
                 lo | (hi << 16);
         } else {

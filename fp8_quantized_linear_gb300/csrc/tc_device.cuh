@@ -172,7 +172,7 @@ __device__ __forceinline__ uint32_t pack_out16(float a, float b, int out_dtype) 
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+__device__ __forceinline__ uint32_t out_e4m3x2(float a, float b) {
     return static_cast<uint32_t>(
         __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
 }

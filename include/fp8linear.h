@@ -52,7 +52,7 @@ extern "C" {
  * 3 adds fp8l_debug_waits, the per-token activation scales
  * (FP8L_A_PER_TOKEN), fp8_rmsnorm_quant and fp8_grouped_mm.  Each change is additive: a caller written for an
  * earlier version runs unchanged. */
-#define FP8L_ABI_VERSION 4
+#define FP8L_ABI_VERSION 5
 
 /* Only the entry points below are exported from the shared library. */
 #if defined(__GNUC__)
@@ -210,6 +210,37 @@ FP8L_API int fp8_scaled_mm(const uint8_t *a, const uint8_t *w, int64_t M, int64_
                   int64_t K, const float *a_scale, const float *w_scale,
                   int w_per_channel, const float *out_scale, void *y,
                   int out_dtype, void *workspace, unsigned flags, void *stream);
+
+/* Largest x (bytes) of a dynamic-scale fp8_quant_scaled_mm: every CTA of the
+ * product reads all of it to take its maximum. */
+#define FP8L_FUSED_DYNAMIC_MAX_BYTES 65536
+
+/* W8A8 product of few tokens with the activation quantization fused into it
+ * ("Condition to achieve linear speedup?": quantization fused into another
+ * kernel instead of its own launch; "RFC: FP8 Quantization Schema in
+ * vLLM": static input scales):
+ *
+ *   dynamic:  a_scale[0] = amax(|x|) / 448 (1 if that is 0), written
+ *   static:   a_scale[0] read
+ *   a = E4M3(x / a_scale[0])  (the codes of fp8_quant_per_tensor, bit for bit)
+ *   y = fp8_scaled_mm(a, w, a_scale, w_scale, ...)
+ *
+ * with the swapped-operand tcgen05 product, in one kernel and without
+ * writing the codes: up to 64 tokens the result is bit-for-bit that of
+ * fp8_quant_per_tensor followed by fp8_scaled_mm with FP8L_KERNEL_SWAPPED
+ * (above, the 16-bit token stages leave room for one CTA per SM, K may be
+ * split over fewer CTAs and the fp32 sums round differently, within the
+ * layer's tolerance).  x: [M, K] of x_dtype
+ * (FP8L_F16 or FP8L_BF16), 0 <= M <= 128 (FP8L_ESHAPE above); a dynamic
+ * scale also needs 2 M K <= FP8L_FUSED_DYNAMIC_MAX_BYTES (every CTA reads
+ * all of x; FP8L_ESHAPE otherwise).  w, w_scale, w_per_channel, out_scale,
+ * y, out_dtype and workspace as for fp8_scaled_mm; per-tensor a_scale only.
+ * flags: FP8L_WEIGHTS_STABLE (other bits are FP8L_EINVAL). */
+FP8L_API int fp8_quant_scaled_mm(const void *x, int x_dtype, const uint8_t *w, int64_t M,
+                                 int64_t N, int64_t K, float *a_scale, int dynamic,
+                                 const float *w_scale, int w_per_channel,
+                                 const float *out_scale, void *y, int out_dtype,
+                                 void *workspace, unsigned flags, void *stream);
 
 /* The kernel fp8_scaled_mm runs for this shape and these flags:
  * FP8L_KERNEL_STREAM, FP8L_KERNEL_SWAPPED or FP8L_KERNEL_TILED (the flags'

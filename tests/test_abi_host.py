@@ -54,7 +54,7 @@ def test_only_c_abi_symbols_exported(lib):
 
 def test_constants(lib):
     import fp8_quantized_linear_gb300 as fl
-    assert lib.fp8l_abi_version() == fl._binding.ABI_VERSION == 4
+    assert lib.fp8l_abi_version() == fl._binding.ABI_VERSION == 5
     assert fl.fp8l_workspace_bytes() >= 4096 and fl.fp8l_workspace_bytes() % 16 == 0
     for code in range(7):
         assert fl.strerror(code)
@@ -113,6 +113,31 @@ def test_scaled_mm_kernel_choice(lib):
     assert k(1024, 4096, 4096) == "tiled"
     for name in ("stream", "swapped", "tiled"):  # an explicit choice is kept
         assert k(1024, 4096, 4096, name) == name
+
+
+def test_quant_scaled_mm_argument_errors(lib):
+    import fp8_quantized_linear_gb300._binding as b
+    f = lib.fp8_quant_scaled_mm
+    ok = dict(x=A16, xd=b.BF16, w=A16, M=16, N=32, K=64, sa=A16, dyn=1, sw=A16, pc=0, os=None,
+              y=A16, od=b.BF16, ws=A16, fl=0, st=None)
+
+    def call(**kw):
+        d = dict(ok)
+        d.update(kw)
+        return f(d["x"], d["xd"], d["w"], d["M"], d["N"], d["K"], d["sa"], d["dyn"], d["sw"], d["pc"],
+                 d["os"], d["y"], d["od"], d["ws"], d["fl"], d["st"])
+    assert call(xd=b.E4M3) == b.EINVAL
+    assert call(xd=b.F32) == b.EINVAL
+    assert call(od=7) == b.EINVAL
+    assert call(fl=2) == b.EINVAL
+    assert call(sa=None) == b.EINVAL
+    assert call(od=b.E4M3, os=None) == b.EINVAL
+    assert call(M=129) == b.ESHAPE
+    assert call(N=24) == b.ESHAPE
+    # dynamic: every CTA reads all of x, so x is bounded
+    assert call(M=4, K=8192 + 16) == b.ESHAPE
+    assert call(x=A16 + 8) == b.EALIGN
+    assert call(sa=A16 + 2) == b.EALIGN
 
 
 def test_w8a16_mm_kernel_choice(lib):

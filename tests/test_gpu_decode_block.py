@@ -1,6 +1,7 @@
 """The Llama-3-8B-shaped decode layer chained through the library and
 captured in one CUDA graph ("Marlin fp8": FP8 decode pays off with CUDA
-graphs).  Each stage is compared with the CPU oracle on the input the GPU
+graphs); at one token the W8A8 layer's o, gate/up and down products run with
+their quantization fused.  Each stage is compared with the CPU oracle on the input the GPU
 gave it, and graph replays must reproduce eager execution bit for bit."""
 import numpy as np
 import pytest
@@ -48,7 +49,8 @@ def test_stages_against_oracle(M, kind, weights):
             else:
                 src = host(inp)
             q_o, s_o = oracle.quant_per_tensor(src.astype(np.float32))
-            assert np.array_equal(host(blk.qa[name]), q_o), name
+            if not blk.fused(name):  # a fused product never writes its codes
+                assert np.array_equal(host(blk.qa[name]), q_o), name
             assert np.float32(host(blk.sa[name])[0]) == s_o, name
             y_ref = oracle.scaled_mm_ref(q_o, qw, s_o, sw)
         assert_gemm_close(host(blk.y[name]), y_ref, (kind, M, name))
