@@ -277,6 +277,12 @@ def w8a8_bytes(M, N, K, out_bytes, per_channel):
     return M * K + N * K + M * N * out_bytes + 4 * (N if per_channel else 1) + 4
 
 
+def fused_bytes(M, N, K, out_bytes, per_channel):
+    """Algorithmic bytes of fp8_quant_scaled_mm: the 16-bit activations,
+    the weights, the output and the scales."""
+    return w8a8_bytes(M, N, K, out_bytes, per_channel) + M * K
+
+
 class Call:
     """One public-API call inside a step (1 or 2 kernel launches)."""
 
@@ -383,6 +389,15 @@ class Workload:
                                 w8a16_bytes(M, N, K), "bytes", 1, (M, N, K)))
                 continue
             dynamic = wl.act_scale == "dynamic"
+            if fl.quant_scaled_mm_preferred(M, N, K, dynamic):
+                # quantization inside the product: 16-bit x read instead of the codes
+                out.append(Call("scaled_mm_fused_quant",
+                                lambda it=it, dyn=dynamic: fl.fp8_quant_scaled_mm(
+                                    it["x"], it["qw"], it["sw"], a_scale=it["sa"], dynamic=dyn,
+                                    out_scale=it.get("os"), y=it["y"], ws=ws, stable_weights=True),
+                                fused_bytes(M, N, K, it["y"].element_size(), wl.w_scale == "channel"),
+                                "bytes", 1, (M, N, K)))
+                continue
             out.append(Call("quant_dynamic" if dynamic else "quant_static",
                             lambda it=it, dyn=dynamic: fl.fp8_quant_per_tensor(
                                 it["x"], q=it["qa"], scale=it["sa"], dynamic=dyn, ws=ws),
@@ -458,6 +473,12 @@ class Workload:
                 if wl.kind == "w8a16":
                     fl.fp8_w8a16_mm(x, it["qw"], it["sw"], y=y, stable_weights=True,
                                     packed=self.packed)
+                elif fl.quant_scaled_mm_preferred(it["M"], it["N"], it["K"],
+                                                  wl.act_scale == "dynamic"):
+                    fl.fp8_quant_scaled_mm(x, it["qw"], it["sw"], a_scale=it["sa"],
+                                           dynamic=wl.act_scale == "dynamic",
+                                           out_scale=it.get("os"), y=y, ws=ws,
+                                           stable_weights=True)
                 else:
                     fl.fp8_quant_per_tensor(x, q=it["qa"], scale=it["sa"],
                                             dynamic=wl.act_scale == "dynamic", ws=ws)
@@ -683,7 +704,7 @@ def roofline(per_kind, peaks, ms_per_step, sustained=False):
 
 
 KERNEL_SOURCES = {"w8a16_skinny": "skinny.cu", "scaled_mm_skinny": "skinny.cu",
-                  "scaled_mm_swapped": "gemm_swapab.cu",
+                  "scaled_mm_swapped": "gemm_swapab.cu", "scaled_mm_fused_quant": "gemm_swapab.cu",
                   "scaled_mm_tcgen05": "gemm_tcgen05.cu", "quant_dynamic": "quant.cu",
                   "quant_static": "quant.cu"}
 
@@ -1015,7 +1036,8 @@ def per_shape(work, peaks, steps):
     exceed three L2 sizes, so each call reads from HBM), and is replayed back
     to back between two CUDA events: no host dispatch or tensor-map encoding
     falls inside the timed window.  W8A8 shapes also time their activation
-    quantization the same way.  The roofline of each product is
+    quantization the same way, and the fused quantization + product where the
+    step uses it (fused_us).  The roofline of each product is
     min(peak, HBM x AI): the FP8 tensor peak for W8A8, the 16-bit one for
     W8A16."""
     fl, wl, dev = work.fl, work.wl, work.device
@@ -1056,7 +1078,7 @@ def per_shape(work, peaks, steps):
             prods = [lambda c=c: fl.fp8_w8a16_mm(c["x"], c["qw"], c["sw"], y=c["y"],
                                                  stable_weights=True, packed=work.packed)
                      for c in copies]
-            quants = []
+            quants, fuseds = [], []
         else:
             dyn = wl.act_scale == "dynamic"
             quants = [lambda c=c: fl.fp8_quant_per_tensor(c["x"], q=c["qa"], scale=c["sa"],
@@ -1066,8 +1088,12 @@ def per_shape(work, peaks, steps):
                                                   y=c["y"], ws=ws, stable_weights=True,
                                                   single_sm=Workload.single_sm)
                      for c in copies]
+            fuseds = ([lambda c=c: fl.fp8_quant_scaled_mm(c["x"], c["qw"], c["sw"], a_scale=c["sa"],
+                                                          dynamic=dyn, out_scale=c.get("os"),
+                                                          y=c["y"], ws=ws, stable_weights=True)
+                       for c in copies] if fl.quant_scaled_mm_preferred(M, N, K, dyn) else [])
         with torch.cuda.stream(stream):  # eager pass: quantized activations, library set-up
-            for fn in quants + prods:
+            for fn in fuseds + quants + prods:
                 fn()
         stream.synchronize()
         sec = timed(prods)
@@ -1078,8 +1104,13 @@ def per_shape(work, peaks, steps):
             qsec = timed(quants)
             row["quant_us"] = round(qsec * 1e6, 2)
             row["quant_hbm_frac"] = round(3 * M * K / qsec / 1e9 / peaks["hbm_gbs"], 4)
+        if fuseds:  # the call the step makes: quantization inside the product
+            fsec = timed(fuseds)
+            fb = fused_bytes(M, N, K, base["y"].element_size(), wl.w_scale == "channel")
+            row["fused_us"] = round(fsec * 1e6, 2)
+            row["fused_hbm_frac"] = round(fb / fsec / 1e9 / peaks["hbm_gbs"], 4)
         rows.append(row)
-        del copies, prods, quants
+        del copies, prods, quants, fuseds
     torch.cuda.synchronize(dev)
     return rows
 

@@ -17,7 +17,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfp8linear.so")
 
-ABI_VERSION = 5  # the library version this binding is written for
+ABI_VERSION = 6  # the library version this binding is written for
 F16, BF16, E4M3, F32 = 0, 1, 2, 3
 WEIGHTS_STABLE = 1
 WEIGHTS_PACKED = 2
@@ -78,6 +78,8 @@ def load():
         lib.fp8_quant_scaled_mm.restype = I
         lib.fp8_quant_scaled_mm.argtypes = [P, I, P, I64, I64, I64, P, I, P, I, P, P, I, P,
                                             ctypes.c_uint, P]
+        lib.fp8_quant_scaled_mm_preferred.restype = I
+        lib.fp8_quant_scaled_mm_preferred.argtypes = [I64, I64, I64, I]
         lib.fp8_w8a16_mm_kernel.restype = ctypes.c_uint
         lib.fp8_w8a16_mm_kernel.argtypes = [I64, I64, I64, ctypes.c_uint]
         lib.fp8_scaled_mm_kernel.restype = ctypes.c_uint
@@ -243,6 +245,12 @@ def scaled_mm_kernel(M: int, N: int, K: int, kernel: str = "auto") -> str:
     for this shape and kernel choice (fp8_scaled_mm_kernel; no GPU needed)."""
     code = load().fp8_scaled_mm_kernel(M, N, K, KERNELS[kernel])
     return {v: k for k, v in KERNELS.items()}[code]
+
+
+def quant_scaled_mm_preferred(M: int, N: int, K: int, dynamic: bool = True) -> bool:
+    """Whether fp8_quant_scaled_mm takes this shape and is the faster way to
+    run it (fp8_quant_scaled_mm_preferred; no GPU needed)."""
+    return bool(load().fp8_quant_scaled_mm_preferred(M, N, K, 1 if dynamic else 0))
 
 
 def fp8_quant_scaled_mm(x: torch.Tensor, w: torch.Tensor, w_scale: torch.Tensor,

@@ -21,8 +21,8 @@ each product's input a function of the previous output).
     quantization before q/k/v (fp8_rmsnorm_quant) and the W8A8 product
     (fp8_scaled_mm) with per-channel weight scales, bf16 outputs; before o,
     gate/up and down the dynamic quantization runs inside the product
-    (fp8_quant_scaled_mm) when the activations are small enough for every
-    CTA to read them (a few tokens), else as its own launch
+    (fp8_quant_scaled_mm) where quant_scaled_mm_preferred says that is the
+    faster way (a few tokens), else as its own launch
     (fp8_quant_per_tensor).
 
 Every call goes through the binding to the library's kernels; this module
@@ -106,10 +106,11 @@ class DecodeBlock:
 
     def fused(self, name: str) -> bool:
         """Whether the product `name` runs with its quantization fused (W8A8,
-        not q/k/v, activations within FUSED_DYNAMIC_MAX_BYTES)."""
-        K = SHAPES[name][1]
+        not q/k/v, where quant_scaled_mm_preferred says the fused call is the
+        faster one)."""
+        N, K = SHAPES[name]
         return (self.kind == "w8a8" and name != "qkv" and
-                2 * self.M * K <= b.FUSED_DYNAMIC_MAX_BYTES)
+                b.quant_scaled_mm_preferred(self.M, N, K, dynamic=True))
 
     def launches(self) -> int:
         """Kernel launches of one forward()."""

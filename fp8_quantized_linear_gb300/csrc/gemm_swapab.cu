@@ -359,13 +359,19 @@ gemm_f8_swapab(const __grid_constant__ CUtensorMap tmap_w,
 //               (24 KB).
 // Every weight stage and token stage has one consumer in k-block order (no
 // barrier can be waited on two phases ahead).
-// Token ring: as many stages as fit kSqXRingBytes, 2 to kSqMaxXStages (with
-// two stages a CTA streaming 32 k-blocks waited on its token loads: 34 us
-// against 25 us for quantizer + product at M = 1, N = 28672).  Above 64
-// tokens the ring takes the shared memory past two CTAs per SM: one CTA per
-// SM then, up to kSqSmemMax.
+// Token ring: kSqXRingBytes, 2 to kSqMaxXStages stages (with two stages a
+// CTA streaming 32 k-blocks waited on its token loads: 34 us against 25 us
+// for quantizer + product at M = 1, N = 28672; at 16 tokens 4 weight and 6
+// token stages beat 5 and 5).  Weight ring: the rest of kSqSmemTarget, two
+// CTAs per SM (233472 bytes of shared memory per SM, 1024 reserved per CTA,
+// 512 left for the kernel's static shared variables: a CTA 20 bytes over
+// the limit ran one per SM and took 1.7x as long).  Above 64 tokens the
+// rings take the shared memory past two CTAs per SM: one CTA per SM then,
+// up to kSqSmemMax.
 constexpr int kSqMaxXStages = 16;
+constexpr int kSqMinXStagesTrade = 8;
 constexpr size_t kSqXRingBytes = 24 * 1024;
+constexpr size_t kSqSmemTarget = 233472 / 2 - 1024 - 512;
 constexpr size_t kSqSmemMax = 220 * 1024;
 constexpr int kSqConvThreads = 64;
 // warp 4 loads the tokens: in lane 1 of the weight producer's warp its
@@ -1413,14 +1419,34 @@ int launch_swapab_q(const void *x, int x_dtype, const uint8_t *w, int M, int N, 
     p.T = (M + 15) & ~15;
     p.stage_bytes = kSwWBytes + p.T * SW_BK;
     const size_t xsb = size_t(M) * 256;
+    // token ring first (kSqXRingBytes, 2 to kSqMaxXStages stages), weight
+    // stages in the rest of kSqSmemTarget; then, if that is fewer weight
+    // stages than the plain swapped product keeps in flight, the token ring
+    // gives up stages to match it as long as kSqMinXStagesTrade remain
+    const size_t fixed = 1024 + 64;
+    const size_t per_w = p.stage_bytes + 24, per_x = xsb + 16;
     int xst = static_cast<int>(kSqXRingBytes / xsb);
     if (xst > kSqMaxXStages) xst = kSqMaxXStages;
     if (xst < 2) xst = 2;
-    p.x_stages = xst;
-    const size_t xring = size_t(xst) * xsb;
-    int stages = static_cast<int>((size_t(kSwSmemTarget) - 1024 - 64 - 16 * xst - xring) / (p.stage_bytes + 24));
+    auto w_room = [&](int xs) {
+        const size_t used = fixed + size_t(xs) * per_x;
+        return used >= kSqSmemTarget ? 0 : static_cast<int>((kSqSmemTarget - used) / per_w);
+    };
+    int stages = w_room(xst);
+    int plain = static_cast<int>((kSwSmemTarget - 1024 - 24) / (p.stage_bytes + 16));
+    if (plain > kSwMaxStages) plain = kSwMaxStages;
+    if (stages < plain) {
+        const size_t need = fixed + size_t(plain) * per_w;
+        const int xs = need >= kSqSmemTarget ? 0 : static_cast<int>((kSqSmemTarget - need) / per_x);
+        if (xs >= kSqMinXStagesTrade && xs < xst) {
+            xst = xs;
+            stages = plain;
+        }
+    }
     if (stages > kSwMaxStages) stages = kSwMaxStages;
     if (stages < 3) stages = 3;
+    p.x_stages = xst;
+    const size_t xring = size_t(xst) * xsb;
     p.stages = stages;
     const size_t ring = size_t(stages) * p.stage_bytes + xring;
     const size_t smem = 1024 + ((ring + 7) & ~size_t(7)) + size_t(3 * stages + 2 * xst + 1) * 8 + 16;
@@ -1480,6 +1506,25 @@ int launch_swapab_q(const void *x, int x_dtype, const uint8_t *w, int M, int N, 
 }
 
 }  // namespace fp8l
+
+// Weight blocks (128 rows) up to which the fused product was measured
+// faster than quantizer + product on a 152-SM GB300: up to 8 tokens while
+// every block has a CTA in the first wave (2 per SM), 9-16 tokens while the
+// blocks are few enough for clusters to split K (one per SM or fewer).
+// Beyond that the fused kernel's CTAs, with fewer weight stages and a
+// conversion step in each stage's round trip, stream too slowly alone
+// (M = 1 at 57344 x 8192: 88 us against 80; M = 16 at 28672 x 4096: 29.3
+// against 27.3; M = 32 at 6144 x 4096: 14.3 against 13.5).
+constexpr int64_t kFusedPreferBlocks = 152;
+
+extern "C" int fp8_quant_scaled_mm_preferred(int64_t M, int64_t N, int64_t K, int dynamic) {
+    using namespace fp8l;
+    if (M < 1 || M > 16 || N <= 0 || K <= 0 || N > (1 << 20) || K > (1 << 20) || N % 16 != 0 || K % 16 != 0)
+        return 0;
+    if (dynamic && M * K * 2 > FP8L_FUSED_DYNAMIC_MAX_BYTES) return 0;
+    const int64_t blocks = (N + SW_BM - 1) / SW_BM;
+    return blocks <= (M <= 8 ? 2 : 1) * kFusedPreferBlocks ? 1 : 0;
+}
 
 extern "C" int fp8_quant_scaled_mm(const void *x, int x_dtype, const uint8_t *w, int64_t M, int64_t N,
                                    int64_t K, float *a_scale, int dynamic, const float *w_scale,

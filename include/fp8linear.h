@@ -52,7 +52,7 @@ extern "C" {
  * 3 adds fp8l_debug_waits, the per-token activation scales
  * (FP8L_A_PER_TOKEN), fp8_rmsnorm_quant and fp8_grouped_mm.  Each change is additive: a caller written for an
  * earlier version runs unchanged. */
-#define FP8L_ABI_VERSION 5
+#define FP8L_ABI_VERSION 6
 
 /* Only the entry points below are exported from the shared library. */
 #if defined(__GNUC__)
@@ -241,6 +241,16 @@ FP8L_API int fp8_quant_scaled_mm(const void *x, int x_dtype, const uint8_t *w, i
                                  const float *w_scale, int w_per_channel,
                                  const float *out_scale, void *y, int out_dtype,
                                  void *workspace, unsigned flags, void *stream);
+
+/* 1 when fp8_quant_scaled_mm accepts this shape (dynamic: the scale is
+ * taken in the call) and was measured faster on a GB300 than
+ * fp8_quant_per_tensor followed by fp8_scaled_mm, else 0: up to 8 tokens
+ * with at most 304 blocks of 128 weight rows, 9 to 16 tokens with at most
+ * 152 (beyond, every CTA converts all the tokens of its K range itself, and
+ * with fewer weight stages in flight than the plain product a CTA streams
+ * its weights more slowly).  A pure function of its arguments; needs no
+ * GPU. */
+FP8L_API int fp8_quant_scaled_mm_preferred(int64_t M, int64_t N, int64_t K, int dynamic);
 
 /* The kernel fp8_scaled_mm runs for this shape and these flags:
  * FP8L_KERNEL_STREAM, FP8L_KERNEL_SWAPPED or FP8L_KERNEL_TILED (the flags'

@@ -54,7 +54,7 @@ def test_only_c_abi_symbols_exported(lib):
 
 def test_constants(lib):
     import fp8_quantized_linear_gb300 as fl
-    assert lib.fp8l_abi_version() == fl._binding.ABI_VERSION == 5
+    assert lib.fp8l_abi_version() == fl._binding.ABI_VERSION == 6
     assert fl.fp8l_workspace_bytes() >= 4096 and fl.fp8l_workspace_bytes() % 16 == 0
     for code in range(7):
         assert fl.strerror(code)
@@ -113,6 +113,28 @@ def test_scaled_mm_kernel_choice(lib):
     assert k(1024, 4096, 4096) == "tiled"
     for name in ("stream", "swapped", "tiled"):  # an explicit choice is kept
         assert k(1024, 4096, 4096, name) == name
+
+
+def test_quant_scaled_mm_preferred(lib):
+    # when the fused quantization + product is the faster call: a pure
+    # function of the shape, no GPU
+    import fp8_quantized_linear_gb300 as fl
+    p = fl.quant_scaled_mm_preferred
+    assert p(1, 28672, 4096)                  # 224 weight blocks, one wave at 8 tokens or fewer
+    assert p(8, 28672, 4096, dynamic=False)
+    assert p(1, 4096, 14336)                  # dynamic: 28 KB of x
+    assert not p(4, 4096, 14336)              # dynamic: 112 KB of x, over the limit
+    assert p(4, 4096, 14336, dynamic=False)
+    assert p(1, 38912, 4096)                  # 304 blocks
+    assert not p(1, 38928, 4096)              # 305 blocks: a second wave
+    assert not p(1, 57344, 8192)
+    assert p(16, 6144, 4096, dynamic=False)   # 48 blocks: clusters split K
+    assert p(16, 19456, 4096, dynamic=False)  # 152 blocks
+    assert not p(16, 19472, 4096, dynamic=False)
+    assert not p(16, 28672, 4096, dynamic=False)
+    assert not p(16, 6144, 4096)              # dynamic: 128 KB of x
+    assert not p(17, 6144, 1024, dynamic=False)
+    assert not p(0, 4096, 4096) and not p(1, 4100, 4096) and not p(1, 4096, 0)
 
 
 def test_quant_scaled_mm_argument_errors(lib):

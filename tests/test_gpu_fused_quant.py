@@ -82,6 +82,50 @@ def test_static_equals_quantizer_then_product(M, N, K, stable):
     _status_ok()
 
 
+_WORKLOAD_CASES = [pytest.param(name, i, id=f"{name}-{M}x{N}x{K}")
+                   for name, wl in synthetic.WORKLOADS.items() if wl.kind == "w8a8"
+                   for i, (M, N, K) in enumerate(wl.shapes) if M <= 16]
+
+
+@pytest.mark.parametrize("name,i", _WORKLOAD_CASES)
+def test_workload_shapes_where_fused_is_preferred(name, i):
+    # every product the benchmark runs as one fused call: its workload's
+    # activations, scale mode, weight scales and output type
+    wl = synthetic.WORKLOADS[name]
+    M, N, K = wl.shapes[i]
+    dynamic = wl.act_scale == "dynamic"
+    if not fl.quant_scaled_mm_preferred(M, N, K, dynamic):
+        pytest.skip("quantizer + product is the faster path for this shape")
+    x = synthetic.activation(M, K, wl.x_dtype, seed=wl.seed(i), outlier_frac=wl.outlier_frac).to(DEV)
+    wd, swd, qw, sw = _weights(N, K, wl.w_scale == "channel", seed=wl.seed(i))
+    if dynamic:
+        qa_o, sa_o = oracle.quant_per_tensor(x.cpu())
+        sa = torch.empty(1, dtype=torch.float32, device=DEV)
+    else:
+        sa_o = np.float32(float(x.abs().max().item()) / 448.0 * 0.75)  # the outliers saturate
+        qa_o, _ = oracle.quant_per_tensor(x.cpu(), scale=sa_o)
+        sa = scalar(sa_o)
+    y_o = oracle.scaled_mm_ref(qa_o, qw, sa_o, sw)
+    e4m3 = wl.out_dtype == "e4m3"
+    od = {"bf16": torch.bfloat16, "fp16": torch.float16, "e4m3": torch.uint8}[wl.out_dtype]
+    os_v = np.float32(np.abs(y_o).max() / 448.0) if e4m3 else None
+    os_ = scalar(os_v) if e4m3 else None
+    y, sa_f = fl.fp8_quant_scaled_mm(x, wd, swd, a_scale=sa, dynamic=dynamic, out_dtype=od,
+                                     out_scale=os_, stable_weights=True)
+    assert np.float32(host(sa_f)[0]) == np.float32(sa_o)
+    qa = torch.empty((M, K), dtype=torch.uint8, device=DEV)
+    sa2 = torch.empty(1, dtype=torch.float32, device=DEV) if dynamic else sa
+    fl.fp8_quant_per_tensor(x, q=qa, scale=sa2, dynamic=dynamic)
+    assert np.array_equal(host(qa).astype(np.uint8), qa_o)
+    y_sep = fl.fp8_scaled_mm(qa, wd, sa2, swd, out_dtype=od, out_scale=os_, kernel="swapped")
+    assert torch.equal(y, y_sep)
+    if e4m3:
+        assert_e4m3_close(host(y), y_o, os_v)
+    else:
+        assert_gemm_close(host(y), y_o)
+    _status_ok()
+
+
 def test_graph_chain():
     # x -> y1 (dynamic) -> y2 = fused(y1) (dynamic) in one CUDA graph, both
     # programmatic dependents; outputs and scales zeroed before each replay
