@@ -171,3 +171,33 @@ def test_long_timed_regions_use_the_sustained_tensor_peak():
     assert sust["frac"] == pytest.approx(3000 / 3381.0, abs=1e-4)
     assert sust["frac_of_burst"] == burst["frac"]
     assert "sustained" in sust["peak_source"] and "burst" in burst["peak_source"]
+
+
+def _two_machine_makespan(order, first, second):
+    t1 = t2 = 0
+    for i in order:
+        t1 += first[i]
+        t2 = max(t2, t1) + second[i]
+    return t2
+
+
+def test_johnson_order_minimizes_the_two_machine_makespan():
+    # brute force over every order of small random instances (ties included)
+    import itertools
+    import random
+    rng = random.Random(5)
+    for _ in range(200):
+        n = rng.randint(1, 6)
+        first = [rng.randint(0, 9) for _ in range(n)]
+        second = [rng.randint(0, 9) for _ in range(n)]
+        order = bench.johnson_order(first, second)
+        assert sorted(order) == list(range(n))
+        best = min(_two_machine_makespan(p, first, second) for p in itertools.permutations(range(n)))
+        assert _two_machine_makespan(order, first, second) == best
+
+
+def test_johnson_order_of_the_headline_copies():
+    # a product with a small input and a large output goes early, one with
+    # a large input and a small output late
+    order = bench.johnson_order([67, 235, 1, 17], [235, 34, 4, 59])
+    assert order == [2, 3, 0, 1]
