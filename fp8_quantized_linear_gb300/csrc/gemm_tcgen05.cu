@@ -57,6 +57,8 @@ constexpr int kTmemCols = 2 * BN;  // two accumulators
 // us for bf16 output and a per-tensor scale (21.2 us with 8 warps), 8192 x
 // 28672 x 4096 737 us against 554.
 constexpr int kEpiWarps = 8;
+constexpr int kEpiGroups = kEpiWarps / 4;  // warps sharing one TMEM lane quarter
+static_assert(kEpiWarps % 4 == 0, "whole groups of four epilogue warps");
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kNumBarriers = 2 * STAGES + 2 + 2 + 1;
 constexpr int kMaxGroups = 256;  // grouped mode: experts
@@ -432,8 +434,8 @@ gemm_f8_tcgen05(const __grid_constant__ CUtensorMap tmap_a,
         __syncwarp();
     } else {
         const int quarter = warp & 3;  // TMEM lanes this warp may read: 32*quarter ..
-        const int half = (warp - 2) >> 2;  // which half of the tile's column chunks
-        const int c_begin = half * (BN / 64), c_end = c_begin + BN / 64;
+        const int grp = (warp - 2) >> 2;  // its share of the tile's 32-column chunks
+        const int c_begin = grp * (BN / 32) / kEpiGroups, c_end = (grp + 1) * (BN / 32) / kEpiGroups;
         const int row = quarter * 32 + lane;
         const float sa0 = __ldg(p.a_scale);
         const float sw0 = __ldg(p.w_scale);
@@ -737,7 +739,7 @@ gemm_f8_pair(const __grid_constant__ CUtensorMap tmap_a,
         __syncwarp();
     } else {
         const int quarter = warp & 3;  // the TMEM lanes this warp may read
-        const int half = (warp - 2) >> 2;
+        const int grp = (warp - 2) >> 2;  // its share of each tile's 32-column chunks
         const int row = static_cast<int>(rank) * P_BM + quarter * 32 + lane;  // row in the pair tile
         const float sa0 = __ldg(p.a_scale);
         const float sw0 = __ldg(p.w_scale);
@@ -754,9 +756,9 @@ gemm_f8_pair(const __grid_constant__ CUtensorMap tmap_a,
             const float sa_sw = sa * sw0;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * P_BN);
-            const int chunks = t.w / 32, c_mid = (chunks + 1) / 2;
+            const int chunks = t.w / 32;
 #pragma unroll 1
-            for (int c = half ? c_mid : 0; c < (half ? chunks : c_mid); ++c) {
+            for (int c = grp * chunks / kEpiGroups; c < (grp + 1) * chunks / kEpiGroups; ++c) {
                 uint32_t r[32];
                 tmem_ld32(taddr + static_cast<uint32_t>(c * 32), r);
                 const int n0 = t.n0 + c * 32;
