@@ -32,11 +32,13 @@ def _weights(N, K, per_channel, seed):
     return torch.from_numpy(qw).to(DEV), torch.from_numpy(np.asarray(sw, np.float32)).to(DEV), qw, sw
 
 
-# dynamic scale: every CTA reads all of x (at most 64 KB)
+# dynamic scale: every CTA reads all of x (at most 64 KB); K = 16: one
+# partial k-block, 80 and 208: a ragged last one, N = 16 and 48: one partial
+# weight block
 @pytest.mark.parametrize("xdtype", [torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("out", ["bf16", "e4m3"])
 @pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (1, 2320, 14336), (3, 6144, 4096), (16, 512, 2048),
-                                   (1, 28672, 4096)])
+                                   (1, 28672, 4096), (2, 16, 16), (5, 48, 80), (13, 144, 208)])
 def test_dynamic_equals_quantizer_then_product(M, N, K, out, xdtype):
     x = synthetic.activation(M, K, xdtype, seed=M + N + K, outlier_frac=0.01).to(DEV)
     wd, swd, qw, sw = _weights(N, K, out == "e4m3", seed=N)
