@@ -17,7 +17,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfp8linear.so")
 
-ABI_VERSION = 6  # the library version this binding is written for
+ABI_VERSION = 7  # the library version this binding is written for
 F16, BF16, E4M3, F32 = 0, 1, 2, 3
 WEIGHTS_STABLE = 1
 WEIGHTS_PACKED = 2
@@ -257,11 +257,12 @@ def fp8_quant_scaled_mm(x: torch.Tensor, w: torch.Tensor, w_scale: torch.Tensor,
                         a_scale: torch.Tensor | None = None, dynamic: bool = True,
                         out_dtype=torch.bfloat16, out_scale: torch.Tensor | None = None,
                         y: torch.Tensor | None = None, ws: torch.Tensor | None = None,
-                        stable_weights: bool = False):
+                        stable_weights: bool = False, kernel: str = "auto"):
     """W8A8 product of 16-bit x [M <= 128, K] and E4M3 w [N, K] with the
     per-tensor activation quantization fused into it (fp8_quant_scaled_mm):
     dynamic writes a_scale (a new [1] tensor when None), static reads it.
-    Returns (y, a_scale)."""
+    kernel: "auto" (the one fp8_scaled_mm would run, tiles excepted),
+    "stream" (up to 16 tokens) or "swapped".  Returns (y, a_scale)."""
     _need_cuda(x, w, w_scale, a_scale, out_scale, y, ws)
     w = _codes(w)
     M, K = x.shape
@@ -286,8 +287,8 @@ def fp8_quant_scaled_mm(x: torch.Tensor, w: torch.Tensor, w_scale: torch.Tensor,
             x.data_ptr(), _DTYPE_CODE[x.dtype], w.data_ptr(), M, N, K, a_scale.data_ptr(),
             1 if dynamic else 0, w_scale.data_ptr(), per_channel,
             out_scale.data_ptr() if out_scale is not None else None, _codes(y).data_ptr(),
-            _DTYPE_CODE[y.dtype], ws.data_ptr(), WEIGHTS_STABLE if stable_weights else 0,
-            _stream(x.device))
+            _DTYPE_CODE[y.dtype], ws.data_ptr(),
+            (WEIGHTS_STABLE if stable_weights else 0) | KERNELS[kernel], _stream(x.device))
     _check(st, "fp8_quant_scaled_mm")
     return y, a_scale
 

@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfp8linear.so")
 
-SOURCES = ["api.cu", "quant.cu", "norm_quant.cu", "skinny.cu", "gemm_tcgen05.cu", "gemm_swapab.cu"]
+SOURCES = ["api.cu", "quant.cu", "norm_quant.cu", "skinny.cu", "skinny_quant.cu", "gemm_tcgen05.cu",
+           "gemm_swapab.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", f"-I{INCLUDE}"]

@@ -113,6 +113,12 @@ int launch_skinny_e4m3(const uint8_t *a, const uint8_t *w, int M, int N, int K,
                        const float *a_scale, int a_per_token, const float *w_scale,
                        int w_per_channel, const float *out_scale, void *y, int out_dtype,
                        bool stable_weights, cudaStream_t stream);
+// W8A8 for up to 16 tokens of 16-bit x, the per-tensor quantization (static
+// a_scale read, or dynamic a_scale written) in the weight-streaming kernel
+int launch_skinny_quant(const void *x, int x_dtype, const uint8_t *w, int M, int N, int K,
+                        float *a_scale, int dynamic, const float *w_scale, int w_per_channel,
+                        const float *out_scale, void *y, int out_dtype, bool stable_weights,
+                        cudaStream_t stream);
 int launch_w8a16_tc(const void *x, int x_dtype, const uint8_t *w, bool packed, const float *w_scale,
                     int M, int N, int K, void *y, unsigned *status, int sms, bool stable,
                     cudaStream_t stream);

@@ -1516,12 +1516,18 @@ int launch_swapab_q(const void *x, int x_dtype, const uint8_t *w, int M, int N, 
 // (M = 1 at 57344 x 8192: 88 us against 80; M = 16 at 28672 x 4096: 29.3
 // against 27.3; M = 32 at 6144 x 4096: 14.3 against 13.5).
 constexpr int64_t kFusedPreferBlocks = 152;
+constexpr int64_t kFusedPreferStreamElems = 16384;
 
 extern "C" int fp8_quant_scaled_mm_preferred(int64_t M, int64_t N, int64_t K, int dynamic) {
     using namespace fp8l;
     if (M < 1 || M > 16 || N <= 0 || K <= 0 || N > (1 << 20) || K > (1 << 20) || N % 16 != 0 || K % 16 != 0)
         return 0;
     if (dynamic && M * K * 2 > FP8L_FUSED_DYNAMIC_MAX_BYTES) return 0;
+    if (fp8_scaled_mm_kernel(M, N, K, 0u) == FP8L_KERNEL_STREAM)
+        // the weight stream with the codes made in the kernel: up to 8 tokens
+        // (one token tile), or short rows (the tiny 16 x 512 layer: 2.6 us
+        // against 6.0); 16 tokens of 4096 took 11.9 us against 11.7
+        return (M <= 8 || M * K <= kFusedPreferStreamElems) ? 1 : 0;
     const int64_t blocks = (N + SW_BM - 1) / SW_BM;
     return blocks <= (M <= 8 ? 2 : 1) * kFusedPreferBlocks ? 1 : 0;
 }
@@ -1533,13 +1539,21 @@ extern "C" int fp8_quant_scaled_mm(const void *x, int x_dtype, const uint8_t *w,
     using namespace fp8l;
     if (x_dtype != FP8L_F16 && x_dtype != FP8L_BF16) return FP8L_EINVAL;
     if (out_dtype != FP8L_F16 && out_dtype != FP8L_BF16 && out_dtype != FP8L_E4M3) return FP8L_EINVAL;
-    if ((flags & ~FP8L_WEIGHTS_STABLE) != 0u) return FP8L_EINVAL;
+    if ((flags & ~(FP8L_WEIGHTS_STABLE | FP8L_KERNEL_MASK)) != 0u) return FP8L_EINVAL;
+    unsigned kernel = flags & FP8L_KERNEL_MASK;
+    if (kernel == FP8L_KERNEL_TILED) return FP8L_EINVAL;
     if (a_scale == nullptr || w_scale == nullptr || workspace == nullptr || w == nullptr) return FP8L_EINVAL;
     if (out_dtype == FP8L_E4M3 && out_scale == nullptr) return FP8L_EINVAL;
     if (M < 0 || M > 128 || N <= 0 || K <= 0 || N > (1 << 20) || K > (1 << 20) || N % 16 != 0 ||
         K % 16 != 0)
         return FP8L_ESHAPE;
     if (dynamic && M * K * 2 > FP8L_FUSED_DYNAMIC_MAX_BYTES) return FP8L_ESHAPE;
+    // the kernel fp8_scaled_mm would run the codes through (its tile kernel
+    // excepted): the same MMAs, so the same result
+    if (kernel == FP8L_KERNEL_AUTO)
+        kernel = fp8_scaled_mm_kernel(M, N, K, 0u) == FP8L_KERNEL_STREAM ? FP8L_KERNEL_STREAM
+                                                                        : FP8L_KERNEL_SWAPPED;
+    if (kernel == FP8L_KERNEL_STREAM && M > 16) return FP8L_ESHAPE;
     if (M > 0 && (x == nullptr || y == nullptr)) return FP8L_EINVAL;
     auto misaligned4 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) != 0; };
     if (!aligned16(w) || !aligned16(workspace) || (M > 0 && (!aligned16(x) || !aligned16(y))) ||
@@ -1549,6 +1563,11 @@ extern "C" int fp8_quant_scaled_mm(const void *x, int x_dtype, const uint8_t *w,
     int st = check_device(&sms);
     if (st != FP8L_OK) return st;
     if (M == 0) return FP8L_OK;
+    if (kernel == FP8L_KERNEL_STREAM)
+        return launch_skinny_quant(x, x_dtype, w, static_cast<int>(M), static_cast<int>(N),
+                                   static_cast<int>(K), a_scale, dynamic ? 1 : 0, w_scale,
+                                   w_per_channel ? 1 : 0, out_scale, y, out_dtype,
+                                   (flags & FP8L_WEIGHTS_STABLE) != 0u, as_stream(stream));
     return launch_swapab_q(x, x_dtype, w, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
                            a_scale, dynamic ? 1 : 0, w_scale, w_per_channel ? 1 : 0, out_scale, y, out_dtype,
                            status_word(workspace), sms, (flags & FP8L_WEIGHTS_STABLE) != 0u, as_stream(stream));

@@ -52,7 +52,7 @@ extern "C" {
  * 3 adds fp8l_debug_waits, the per-token activation scales
  * (FP8L_A_PER_TOKEN), fp8_rmsnorm_quant and fp8_grouped_mm.  Each change is additive: a caller written for an
  * earlier version runs unchanged. */
-#define FP8L_ABI_VERSION 6
+#define FP8L_ABI_VERSION 7
 
 /* Only the entry points below are exported from the shared library. */
 #if defined(__GNUC__)
@@ -225,17 +225,23 @@ FP8L_API int fp8_scaled_mm(const uint8_t *a, const uint8_t *w, int64_t M, int64_
  *   a = E4M3(x / a_scale[0])  (the codes of fp8_quant_per_tensor, bit for bit)
  *   y = fp8_scaled_mm(a, w, a_scale, w_scale, ...)
  *
- * with the swapped-operand tcgen05 product, in one kernel and without
- * writing the codes: up to 64 tokens the result is bit-for-bit that of
- * fp8_quant_per_tensor followed by fp8_scaled_mm with FP8L_KERNEL_SWAPPED
- * (above, the 16-bit token stages leave room for one CTA per SM, K may be
- * split over fewer CTAs and the fp32 sums round differently, within the
- * layer's tolerance).  x: [M, K] of x_dtype
+ * in one kernel and without writing the codes: the kernel fp8_scaled_mm
+ * runs for the shape (fp8_scaled_mm_kernel; its token x channel tiles
+ * excepted, which become the swapped-operand product) with the codes made
+ * from x inside it, so up to 64 tokens the result is bit-for-bit that of
+ * fp8_quant_per_tensor followed by fp8_scaled_mm with the same kernel
+ * choice (above, the 16-bit token stages of the swapped-operand product
+ * leave room for one CTA per SM, K may be split over fewer CTAs and the
+ * fp32 sums round differently, within the layer's tolerance).  x: [M, K] of
+ * x_dtype
  * (FP8L_F16 or FP8L_BF16), 0 <= M <= 128 (FP8L_ESHAPE above); a dynamic
  * scale also needs 2 M K <= FP8L_FUSED_DYNAMIC_MAX_BYTES (every CTA reads
  * all of x; FP8L_ESHAPE otherwise).  w, w_scale, w_per_channel, out_scale,
  * y, out_dtype and workspace as for fp8_scaled_mm; per-tensor a_scale only.
- * flags: FP8L_WEIGHTS_STABLE (other bits are FP8L_EINVAL). */
+ * flags: FP8L_WEIGHTS_STABLE and one of FP8L_KERNEL_STREAM (the CUDA-core
+ * weight stream, up to 16 tokens: FP8L_ESHAPE above) or
+ * FP8L_KERNEL_SWAPPED (other bits, FP8L_KERNEL_TILED among them, are
+ * FP8L_EINVAL). */
 FP8L_API int fp8_quant_scaled_mm(const void *x, int x_dtype, const uint8_t *w, int64_t M,
                                  int64_t N, int64_t K, float *a_scale, int dynamic,
                                  const float *w_scale, int w_per_channel,
@@ -244,12 +250,13 @@ FP8L_API int fp8_quant_scaled_mm(const void *x, int x_dtype, const uint8_t *w, i
 
 /* 1 when fp8_quant_scaled_mm accepts this shape (dynamic: the scale is
  * taken in the call) and was measured faster on a GB300 than
- * fp8_quant_per_tensor followed by fp8_scaled_mm, else 0: up to 8 tokens
- * with at most 304 blocks of 128 weight rows, 9 to 16 tokens with at most
- * 152 (beyond, every CTA converts all the tokens of its K range itself, and
- * with fewer weight stages in flight than the plain product a CTA streams
- * its weights more slowly).  A pure function of its arguments; needs no
- * GPU. */
+ * fp8_quant_per_tensor followed by fp8_scaled_mm, else 0.  On the
+ * swapped-operand product: up to 8 tokens with at most 304 blocks of 128
+ * weight rows, 9 to 16 tokens with at most 152 (beyond, every CTA converts
+ * all the tokens of its K range itself, and with fewer weight stages in
+ * flight than the plain product a CTA streams its weights more slowly).  On
+ * the CUDA-core weight stream (small weights): up to 8 tokens, or
+ * M * K <= 16384.  A pure function of its arguments; needs no GPU. */
 FP8L_API int fp8_quant_scaled_mm_preferred(int64_t M, int64_t N, int64_t K, int dynamic);
 
 /* The kernel fp8_scaled_mm runs for this shape and these flags:

@@ -54,7 +54,7 @@ def test_only_c_abi_symbols_exported(lib):
 
 def test_constants(lib):
     import fp8_quantized_linear_gb300 as fl
-    assert lib.fp8l_abi_version() == fl._binding.ABI_VERSION == 6
+    assert lib.fp8l_abi_version() == fl._binding.ABI_VERSION == 7
     assert fl.fp8l_workspace_bytes() >= 4096 and fl.fp8l_workspace_bytes() % 16 == 0
     for code in range(7):
         assert fl.strerror(code)
@@ -134,6 +134,10 @@ def test_quant_scaled_mm_preferred(lib):
     assert not p(16, 28672, 4096, dynamic=False)
     assert not p(16, 6144, 4096)              # dynamic: 128 KB of x
     assert not p(17, 6144, 1024, dynamic=False)
+    # small weights, the CUDA-core weight stream: one token tile, or short rows
+    assert p(8, 4096, 4096, dynamic=False) and p(1, 4096, 4096)
+    assert not p(16, 4096, 4096, dynamic=False)
+    assert p(16, 256, 512)                    # the tiny layer
     assert not p(0, 4096, 4096) and not p(1, 4100, 4096) and not p(1, 4096, 0)
 
 
@@ -154,6 +158,8 @@ def test_quant_scaled_mm_argument_errors(lib):
     assert call(fl=2) == b.EINVAL
     assert call(sa=None) == b.EINVAL
     assert call(od=b.E4M3, os=None) == b.EINVAL
+    assert call(fl=b.KERNELS["tiled"]) == b.EINVAL
+    assert call(fl=b.KERNELS["stream"], M=17, dyn=0) == b.ESHAPE
     assert call(M=129) == b.ESHAPE
     assert call(N=24) == b.ESHAPE
     # dynamic: every CTA reads all of x, so x is bounded

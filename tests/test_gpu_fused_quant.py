@@ -1,10 +1,12 @@
 """GPU parity of fp8_quant_scaled_mm: the per-tensor activation quantization
-fused into the swapped-operand product ("Condition to achieve linear
-speedup?": quantization fused into another kernel; "RFC: FP8 Quantization
-Schema in vLLM": static input scales).  Up to 64 tokens the fused call
-must equal, bit for bit, the quantizer followed by the product (same codes,
-same MMAs, same split of K); its scale and result must match the CPU oracle:
-the dynamic scale exactly, the product within the layer's tolerance."""
+fused into the W8A8 product ("Condition to achieve linear speedup?":
+quantization fused into another kernel; "RFC: FP8 Quantization Schema in
+vLLM": static input scales), in the swapped-operand tcgen05 product or, up
+to 16 tokens, the CUDA-core weight stream.  Up to 64 tokens the fused call
+must equal, bit for bit, the quantizer followed by the product with the
+same kernel choice (same codes, same MMAs, same split of K); its scale and
+result must match the CPU oracle: the dynamic scale exactly, the product
+within the layer's tolerance."""
 import numpy as np
 import pytest
 import torch
@@ -35,19 +37,25 @@ def _weights(N, K, per_channel, seed):
 # dynamic scale: every CTA reads all of x (at most 64 KB); K = 16: one
 # partial k-block, 80 and 208: a ragged last one, N = 16 and 48: one partial
 # weight block
+@pytest.mark.parametrize("kernel", ["auto", "stream", "swapped"])
 @pytest.mark.parametrize("xdtype", [torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("out", ["bf16", "e4m3"])
 @pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (1, 2320, 14336), (3, 6144, 4096), (16, 512, 2048),
                                    (1, 28672, 4096), (2, 16, 16), (5, 48, 80), (13, 144, 208)])
-def test_dynamic_equals_quantizer_then_product(M, N, K, out, xdtype):
+def test_dynamic_equals_quantizer_then_product(M, N, K, out, xdtype, kernel):
+    if kernel == "stream" and M > 16:
+        pytest.skip("the weight stream takes up to 16 tokens")
     x = synthetic.activation(M, K, xdtype, seed=M + N + K, outlier_frac=0.01).to(DEV)
     wd, swd, qw, sw = _weights(N, K, out == "e4m3", seed=N)
     os_ = scalar(0.05) if out == "e4m3" else None
     od = torch.uint8 if out == "e4m3" else torch.bfloat16
     # the separate path: quantizer, then the same product kernel
     qa, sa = fl.fp8_quant_per_tensor(x)
-    y_ref = fl.fp8_scaled_mm(qa, wd, sa, swd, out_dtype=od, out_scale=os_, kernel="swapped")
-    y, sa_f = fl.fp8_quant_scaled_mm(x, wd, swd, dynamic=True, out_dtype=od, out_scale=os_)
+    ref_kernel = kernel if kernel != "auto" else (
+        "stream" if fl.scaled_mm_kernel(M, N, K) == "stream" else "swapped")
+    y_ref = fl.fp8_scaled_mm(qa, wd, sa, swd, out_dtype=od, out_scale=os_, kernel=ref_kernel)
+    y, sa_f = fl.fp8_quant_scaled_mm(x, wd, swd, dynamic=True, out_dtype=od, out_scale=os_,
+                                     kernel=kernel)
     assert host(sa_f)[0] == host(sa)[0]
     assert torch.equal(y, y_ref)
     # and against the oracle
@@ -64,14 +72,15 @@ def test_dynamic_equals_quantizer_then_product(M, N, K, out, xdtype):
 # static scale: any M up to 128; values beyond 1024 x scale take the clamp
 @pytest.mark.parametrize("stable", [False, True])
 @pytest.mark.parametrize("M,N,K", [(1, 4096, 8192), (16, 6144, 4096), (64, 10240, 1024), (100, 2320, 640),
-                                   (128, 4096, 14336)])
+                                   (128, 4096, 14336), (4, 4096, 4096), (12, 1024, 2048), (2, 4096, 2048)])
 def test_static_equals_quantizer_then_product(M, N, K, stable):
     x = synthetic.activation(M, K, torch.bfloat16, seed=7 * M + K, outlier_frac=0.01).to(DEV)
     wd, swd, qw, sw = _weights(N, K, True, seed=K)
     sa = scalar(float(x.abs().max().item()) / 448.0 * 0.25)  # outliers saturate
     qa = torch.empty((M, K), dtype=torch.uint8, device=DEV)
     fl.fp8_quant_per_tensor(x, q=qa, scale=sa, dynamic=False)
-    y_ref = fl.fp8_scaled_mm(qa, wd, sa, swd, out_dtype=torch.bfloat16, kernel="swapped")
+    ref_kernel = "stream" if fl.scaled_mm_kernel(M, N, K) == "stream" else "swapped"
+    y_ref = fl.fp8_scaled_mm(qa, wd, sa, swd, out_dtype=torch.bfloat16, kernel=ref_kernel)
     y, _ = fl.fp8_quant_scaled_mm(x, wd, swd, a_scale=sa, dynamic=False, out_dtype=torch.bfloat16,
                                   stable_weights=stable)
     if M <= 64:
@@ -119,7 +128,8 @@ def test_workload_shapes_where_fused_is_preferred(name, i):
     sa2 = torch.empty(1, dtype=torch.float32, device=DEV) if dynamic else sa
     fl.fp8_quant_per_tensor(x, q=qa, scale=sa2, dynamic=dynamic)
     assert np.array_equal(host(qa).astype(np.uint8), qa_o)
-    y_sep = fl.fp8_scaled_mm(qa, wd, sa2, swd, out_dtype=od, out_scale=os_, kernel="swapped")
+    ref_kernel = "stream" if fl.scaled_mm_kernel(M, N, K) == "stream" else "swapped"
+    y_sep = fl.fp8_scaled_mm(qa, wd, sa2, swd, out_dtype=od, out_scale=os_, kernel=ref_kernel)
     assert torch.equal(y, y_sep)
     if e4m3:
         assert_e4m3_close(host(y), y_o, os_v)
@@ -128,7 +138,8 @@ def test_workload_shapes_where_fused_is_preferred(name, i):
     _status_ok()
 
 
-def test_graph_chain():
+@pytest.mark.parametrize("kernel", ["stream", "swapped"])
+def test_graph_chain(kernel):
     # x -> y1 (dynamic) -> y2 = fused(y1) (dynamic) in one CUDA graph, both
     # programmatic dependents; outputs and scales zeroed before each replay
     M, K, N = 1, 4096, 4096
@@ -142,8 +153,8 @@ def test_graph_chain():
     ws = fl.workspace(DEV)
 
     def step():
-        fl.fp8_quant_scaled_mm(x, w1, s1, a_scale=a1, y=y1, ws=ws, stable_weights=True)
-        fl.fp8_quant_scaled_mm(y1, w2, s2, a_scale=a2, y=y2, ws=ws, stable_weights=True)
+        fl.fp8_quant_scaled_mm(x, w1, s1, a_scale=a1, y=y1, ws=ws, stable_weights=True, kernel=kernel)
+        fl.fp8_quant_scaled_mm(y1, w2, s2, a_scale=a2, y=y2, ws=ws, stable_weights=True, kernel=kernel)
 
     stream = torch.cuda.Stream(DEV)
     with torch.cuda.stream(stream):
@@ -169,6 +180,9 @@ def test_bounds():
     s = torch.ones(1, dtype=torch.float32, device=DEV)
     with pytest.raises(RuntimeError):  # more than 128 tokens
         fl.fp8_quant_scaled_mm(torch.zeros((129, 64), dtype=torch.bfloat16, device=DEV), w, s)
+    with pytest.raises(RuntimeError):  # the weight stream takes up to 16 tokens
+        fl.fp8_quant_scaled_mm(torch.zeros((17, 64), dtype=torch.bfloat16, device=DEV), w, s,
+                               kernel="stream")
     with pytest.raises(RuntimeError):  # dynamic x larger than 64 KB
         fl.fp8_quant_scaled_mm(torch.zeros((64, 1024), dtype=torch.bfloat16, device=DEV),
                                torch.zeros((64, 1024), dtype=torch.uint8, device=DEV), s)
