@@ -402,8 +402,11 @@ class Workload:
                 continue
             dynamic = wl.act_scale == "dynamic"
             if fl.quant_scaled_mm_preferred(M, N, K, dynamic):
-                # quantization inside the product: 16-bit x read instead of the codes
-                out.append(Call("scaled_mm_fused_quant",
+                # quantization inside the product: 16-bit x read instead of the
+                # codes; in the CUDA-core weight stream for small weights
+                fused_kind = ("scaled_mm_fused_stream" if fl.scaled_mm_kernel(M, N, K) == "stream"
+                              else "scaled_mm_fused_quant")
+                out.append(Call(fused_kind,
                                 lambda it=it, dyn=dynamic: fl.fp8_quant_scaled_mm(
                                     it["x"], it["qw"], it["sw"], a_scale=it["sa"], dynamic=dyn,
                                     out_scale=it.get("os"), y=it["y"], ws=ws, stable_weights=True),
@@ -768,6 +771,7 @@ def roofline(per_kind, peaks, ms_per_step, sustained=False):
 
 KERNEL_SOURCES = {"w8a16_skinny": "skinny.cu", "scaled_mm_skinny": "skinny.cu",
                   "scaled_mm_swapped": "gemm_swapab.cu", "scaled_mm_fused_quant": "gemm_swapab.cu",
+                  "scaled_mm_fused_stream": "skinny_quant.cu",
                   "scaled_mm_tcgen05": "gemm_tcgen05.cu", "quant_dynamic": "quant.cu",
                   "quant_static": "quant.cu"}
 
